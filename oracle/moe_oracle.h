@@ -1,0 +1,133 @@
+/*
+ * Plain fp64 CPU oracle of the DeepSeek-V3-style MoE layer forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this code.  It shares no source with
+ * the CUDA library and must never sit on the product path.
+ *
+ * The method follows the blog post "专家并行(EP)" (expert parallelism):
+ *   section 2.2 (a token's journey): router linear [7168,256] -> logits ->
+ *     top-8 -> dispatch to the experts' owners -> per-expert FFN ->
+ *     combine back -> output = sum_{i in top-8} softmax(logits)[i] *
+ *     expert_output[i] + shared expert output;
+ *   section 2.1: experts laid out in contiguous blocks, one per EP rank,
+ *     shared experts replicated;
+ *   section 6.2: per-expert arrival counts and per-rank load sums;
+ *   section 6.3: redundant experts (256 + 8 slots, 33 per rank), a token may
+ *     use any replica of its expert.
+ * Readings where the post is silent (softmax over all experts without
+ * renormalisation, SwiGLU form, shared gate = 1, tie rule, replica choice by
+ * token parity, replica placement) are stated at each function.
+ *
+ * bf16 values are passed as their raw uint16 bit patterns; every arithmetic
+ * step is in double precision.  All functions are single-threaded, pure
+ * (no globals) and therefore safe to call from several threads at once.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int32_t hidden;        /* H */
+    int32_t inter;         /* I, routed expert SwiGLU width */
+    int32_t n_experts;     /* E, logical routed experts */
+    int32_t top_k;         /* k */
+    int32_t n_shared;      /* shared experts */
+    int32_t inter_shared;  /* I_sh */
+    int32_t n_slots;       /* S = E or E + replicas */
+    int32_t n_blocks;      /* EP blocks (ranks) */
+} oracle_shape;
+
+/* bf16 bit pattern -> double (exact). */
+double oracle_bf16_to_double(uint16_t v);
+
+/* logits[t,e] = sum_h x[t,h] * w_router[e,h] (+ bias[e]).  x [T,H], w_router [E,H]. */
+void oracle_router_logits(const oracle_shape* s, int T, const uint16_t* x,
+                          const uint16_t* w_router, const float* bias, double* logits);
+
+/* Top-k by value (descending, equal values -> lower expert index first) and the
+ * combine weight softmax(logits over all E)[idx], not renormalised. */
+void oracle_topk_softmax(int T, int E, int k, const double* logits, int32_t* idx, double* weight);
+
+/* Home slot of logical expert e (blocks keep their experts in order; with
+ * replicas each block has trailing replica slots). */
+int32_t oracle_home_slot(const oracle_shape* s, int32_t e);
+
+/* slot_of[t*k+j]: replica of idx if the expert has one and t is odd, else home.
+ * Returns the number of assignments with an expert id outside [0,E); they go
+ * to slot S (the invalid bucket). */
+int oracle_slot_map(const oracle_shape* s, int T, const int32_t* idx, const int32_t* replica_of,
+                    int32_t* slot_of);
+
+/* counts[S+1] (index S = invalid bucket) and per-block loads block_counts[n_blocks]. */
+void oracle_histogram(const oracle_shape* s, int n_assign, const int32_t* slot_of, int32_t* counts,
+                      int32_t* block_counts);
+
+/* Counting-sort dispatch: offsets[S+2] exclusive prefix of counts (offsets[S+1] = T*k),
+ * rows of a slot in ascending assignment order; perm[row] = a, inv_perm[a] = row;
+ * x_disp[row] = x[a / k] (byte copy).  x_disp may be NULL. */
+void oracle_dispatch(const oracle_shape* s, int T, const int32_t* slot_of, const int32_t* counts,
+                     const uint16_t* x, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                     uint16_t* x_disp);
+
+/* One SwiGLU FFN on one row: y = W_d (silu(W_g x) * (W_u x)).
+ * w_gate/w_up [I,H] (row-major, nn.Linear), w_down [H,I]; y [H]. */
+void oracle_swiglu_row(int H, int I, const uint16_t* x_row, const uint16_t* w_gate,
+                       const uint16_t* w_up, const uint16_t* w_down, double* y);
+
+/* Shared experts on one row: y = sum_j FFN_j(x) (shared gate taken as 1).
+ * ws_* laid out [n_shared, I_sh, H] / [n_shared, H, I_sh]. */
+void oracle_shared_row(const oracle_shape* s, const uint16_t* x_row, const uint16_t* ws_gate,
+                       const uint16_t* ws_up, const uint16_t* ws_down, double* y);
+
+/* Routed expert outputs of every dispatched row: y_disp[row] = FFN_{slot(row)}(x_disp[row]).
+ * Routed weights slot-major [S,I,H], [S,I,H], [S,H,I]. */
+void oracle_expert_ffn(const oracle_shape* s, int T, const int32_t* offsets, const uint16_t* x_disp,
+                       const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                       double* y_disp);
+
+/* out[t] = sum_{j<k} weight[t,j] * y_disp[inv_perm[t*k+j]] + y_shared[t]. */
+void oracle_combine(const oracle_shape* s, int T, const double* y_disp, const int32_t* inv_perm,
+                    const double* weight, const double* y_shared, double* out);
+
+/* Whole layer.  Every output pointer may be NULL except out [T,H].
+ * Returns the number of invalid expert ids met (0 on a well-formed input). */
+int oracle_moe_forward(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
+                       const float* bias, const int32_t* replica_of,
+                       const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                       const uint16_t* ws_gate, const uint16_t* ws_up, const uint16_t* ws_down,
+                       double* logits, int32_t* idx, double* weight, int32_t* slot_of,
+                       int32_t* counts, int32_t* block_counts, int32_t* offsets, int32_t* perm,
+                       int32_t* inv_perm, double* out);
+
+/* One token's output from its routing: out = sum_j weight[j] * FFN(x; expert j's
+ * weights at w_gate[j], w_up[j], w_down[j]) + shared.  For sampled checks at
+ * full size, where only the experts a token uses are generated. */
+void oracle_token_output(const oracle_shape* s, const uint16_t* x_row, int k,
+                         const double* weight, const uint16_t* const* w_gate,
+                         const uint16_t* const* w_up, const uint16_t* const* w_down,
+                         const uint16_t* ws_gate, const uint16_t* ws_up, const uint16_t* ws_down,
+                         double* out);
+
+/* Replica placement for n_rep redundant slots from per-expert counts[E].
+ * Hot list: the n_rep experts with the largest counts (ties -> lower id).
+ * Each block initially carries the load of its experts, a hot expert's
+ * count halved (half its tokens will use the replica).  For each hot expert
+ * in order, the replica goes to the block with the smallest load among those
+ * without a replica yet and other than its home block (ties -> lower block);
+ * if only its home block is free, there.  The block's load grows by half the
+ * expert's count and the replica takes that block's first free replica slot.
+ * replica_of[E]: slot or -1.  Returns 0, or -1 if the shape has no room. */
+int oracle_plan_replicas(const oracle_shape* s, const int32_t* counts, int n_rep,
+                         int32_t* replica_of);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

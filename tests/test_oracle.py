@@ -1,0 +1,368 @@
+"""Pins of the fp64 CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: library
+routines (torch float64 linear algebra, softmax, SiLU, Python's sort), brute
+force, exact invariants, and the figures printed in the blog post
+"专家并行（EP）" (fixtures under tests/golden/).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import moe_inputs as mi
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bf16(shape, std, seed, tid, expert=0):
+    return mi.normal_bf16(shape, std, seed, tid, expert)
+
+
+def _tiny(**kw):
+    return mi.WORKLOADS["tiny"].with_(**kw)
+
+
+def _tiny_inputs(w, replica_of=None, bias=None):
+    x = mi.hidden_states(w)
+    wr = mi.router_weight(w)
+    wg, wu, wd = mi.stacked_expert_weights(w, replica_of)
+    sg, su, sd = mi.stacked_shared_weights(w)
+    return x, wr, bias, wg, wu, wd, sg, su, sd
+
+
+def _f64(t):
+    return t.to(torch.float64)
+
+
+def _swiglu_torch(x, g, u, d):
+    """SwiGLU MLP from torch library routines in float64."""
+    return F.linear(F.silu(F.linear(x, g)) * F.linear(x, u), d)
+
+
+# ------------------------------------------------------------------ conversions
+
+
+def test_bf16_decoding_fixed_patterns():
+    assert oracle.bf16_to_double(0x3F80) == 1.0
+    assert oracle.bf16_to_double(0xC000) == -2.0
+    assert oracle.bf16_to_double(0x3F81) == 1.0 + 2.0 ** -7
+    assert oracle.bf16_to_double(0x0000) == 0.0
+    assert oracle.bf16_to_double(0x8000) == 0.0
+    assert oracle.bf16_to_double(0x0001) == 2.0 ** -133  # smallest subnormal
+
+
+# ------------------------------------------------------------------ router
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_router_logits_match_float64_matmul(with_bias):
+    w = _tiny(tokens=13, hidden=96, n_experts=24, n_blocks=8, n_slots=24)
+    x = mi.hidden_states(w)
+    wr = mi.router_weight(w)
+    bias = np.linspace(-1.0, 1.0, w.n_experts).astype(np.float32) if with_bias else None
+    got = oracle.router_logits(w, x, wr, bias)
+    ref = (_f64(x) @ _f64(wr).T).numpy()
+    if with_bias:
+        ref = ref + bias.astype(np.float64)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-15)
+
+
+def test_topk_matches_bruteforce_sort_and_softmax():
+    rng = np.random.default_rng(3)
+    T, E, k = 40, 64, 8
+    logits = rng.integers(-20, 20, size=(T, E)).astype(np.float64) / 8.0  # many exact ties
+    idx, wt = oracle.topk_softmax(logits, k)
+    for t in range(T):
+        expect = sorted(range(E), key=lambda e: (-logits[t, e], e))[:k]
+        assert list(idx[t]) == expect
+    p = torch.softmax(torch.from_numpy(logits), dim=-1).numpy()
+    np.testing.assert_allclose(wt, np.take_along_axis(p, idx.astype(np.int64), axis=1), rtol=1e-14)
+
+
+def test_topk_tie_rule_hand_cases():
+    # all equal: the lowest indices win, in ascending order
+    idx, wt = oracle.topk_softmax(np.zeros((1, 8)), 3)
+    assert list(idx[0]) == [0, 1, 2]
+    np.testing.assert_allclose(wt[0], [1 / 8] * 3, rtol=1e-15)
+    # equal maxima at 5 and 2: 2 first, then 5; -0.0 ties with +0.0
+    lg = np.array([[0.0, -1.0, 3.0, -0.0, 1.0, 3.0, 1.0, -2.0]])
+    idx, _ = oracle.topk_softmax(lg, 5)
+    assert list(idx[0]) == [2, 5, 4, 6, 0]
+    idx, _ = oracle.topk_softmax(lg, 6)
+    assert list(idx[0]) == [2, 5, 4, 6, 0, 3]
+
+
+def test_softmax_weights_are_not_renormalised():
+    logits = np.array([[2.0, 1.0, 0.0, -1.0]])
+    _, wt = oracle.topk_softmax(logits, 2)
+    e = np.exp(logits[0])
+    np.testing.assert_allclose(wt[0], e[:2] / e.sum(), rtol=1e-15)
+    assert wt[0].sum() < 1.0
+
+
+# ------------------------------------------------------------------ layout, remap, histogram
+
+
+def _golden_kv(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = [s.strip() for s in line.split("=", 1)]
+            out[key] = [int(v) for v in val.split()]
+    return out
+
+
+def test_worked_example_block_mapping():
+    g = _golden_kv("worked_example_routing.txt")
+    w = mi.WORKLOADS["decode_t32"]
+    assert g["n_experts"] == [w.n_experts] and g["n_blocks"] == [w.n_blocks]
+    idx = np.array([g["experts"]], dtype=np.int32)
+    slot_of, invalid = oracle.slot_map(w, idx)
+    assert invalid == 0
+    epb = w.n_experts // w.n_blocks
+    assert [int(s) // epb for s in slot_of] == g["blocks"]
+    _, blocks = oracle.histogram(w, slot_of)
+    assert list(blocks) == g["block_counts"]
+
+
+def test_home_slots_of_redundant_layout():
+    w = mi.WORKLOADS["redundant_t1024"]  # 264 slots, 33 per block
+    assert [oracle.home_slot(w, e) for e in (0, 31, 32, 33, 255)] == [0, 31, 33, 34, 262]
+    w0 = mi.WORKLOADS["decode_t32"]
+    assert [oracle.home_slot(w0, e) for e in (0, 31, 32, 255)] == [0, 31, 32, 255]
+
+
+def test_slot_map_replica_parity_and_invalid_ids():
+    w = _tiny(n_experts=8, n_blocks=4, n_slots=12, top_k=2)
+    rep = np.full(8, -1, dtype=np.int32)
+    rep[3] = 11  # expert 3 (home block 1, slot 4) replicated in block 3's replica slot
+    idx = np.array([[3, 0], [3, 7], [9, 3], [3, -1]], dtype=np.int32)
+    slot_of, invalid = oracle.slot_map(w, idx, rep)
+    # home(e) = (e // 2) * 3 + e % 2: home(3)=4, home(0)=0, home(7)=10
+    assert list(slot_of) == [4, 0, 11, 10, 12, 4, 11, 12]
+    assert invalid == 2
+    counts, _ = oracle.histogram(w, slot_of)
+    assert counts[12] == 2 and counts.sum() == idx.size
+
+
+def test_histogram_and_dispatch_invariants():
+    w = _tiny(tokens=37, n_experts=16, n_blocks=4, n_slots=16, top_k=3, hidden=24)
+    rng = np.random.default_rng(7)
+    idx = np.stack([rng.choice(w.n_experts, w.top_k, replace=False) for _ in range(w.tokens)]).astype(np.int32)
+    slot_of, invalid = oracle.slot_map(w, idx)
+    assert invalid == 0
+    counts, blocks = oracle.histogram(w, slot_of)
+    n = w.tokens * w.top_k
+    assert counts.sum() == n and counts[-1] == 0
+    assert blocks.sum() == n and list(blocks) == [counts[4 * b:4 * b + 4].sum() for b in range(4)]
+    assert list(counts[:-1]) == list(np.bincount(slot_of, minlength=w.n_slots))
+    x = mi.hidden_states(w)
+    offsets, perm, inv, xd = oracle.dispatch(w, w.tokens, slot_of, counts, x)
+    assert offsets[0] == 0 and offsets[-1] == n and offsets[w.n_slots] == n
+    assert np.all(np.diff(offsets) == counts)
+    assert sorted(perm) == list(range(n))
+    assert np.array_equal(inv[perm], np.arange(n)) and np.array_equal(perm[inv], np.arange(n))
+    for s in range(w.n_slots):
+        seg = perm[offsets[s]:offsets[s + 1]]
+        assert np.all(slot_of[seg] == s)
+        assert np.all(np.diff(seg) > 0)  # stable: ascending assignment index
+    # dispatch then inverse permutation returns every token's row exactly
+    xs = x.view(torch.int16).numpy().view(np.uint16)
+    back = xd[inv].reshape(w.tokens, w.top_k, w.hidden)
+    for j in range(w.top_k):
+        assert np.array_equal(back[:, j, :], xs)
+    assert xd.nbytes == w.tokens * w.top_k * w.hidden * 2
+
+
+def test_payload_bytes_match_pages():
+    rows = {}
+    with open(os.path.join(GOLDEN, "pages_constants.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, exact, printed, unit, _src = [s.strip() for s in line.split("|")]
+            rows[name] = (int(exact), float(printed), unit)
+    w = mi.WORKLOADS["decode_t32"].with_(tokens=1)
+    idx = np.arange(w.top_k, dtype=np.int32)[None, :] * 31
+    slot_of, _ = oracle.slot_map(w, idx)
+    counts, _ = oracle.histogram(w, slot_of)
+    x = mi.hidden_states(w)
+    _, _, _, xd = oracle.dispatch(w, 1, slot_of, counts, x)
+    # dispatch buffer of one token + the equally sized combine payload
+    assert x.numel() * 2 == rows["token_hidden_bytes"][0]
+    assert 2 * xd.nbytes == rows["dispatch_combine_bytes_per_token"][0]
+    assert xd.nbytes == rows["dispatch_combine_bytes_per_token_fp8"][0]  # 1 byte per element
+    unit = {"KB": 1e3, "MB": 1e6, "GB": 1e9}
+    for name, (exact, printed, u) in rows.items():
+        if u in unit:
+            assert abs(exact / unit[u] - printed) / printed < 0.03, name
+    per_expert = 3 * w.hidden * w.inter * 2
+    assert per_expert == rows["expert_bytes_fp16"][0]
+    assert w.n_experts * per_expert == rows["routed_expert_bytes_fp16"][0]
+    assert w.n_shared * 3 * w.hidden * w.inter_shared * 2 == rows["shared_expert_bytes_fp16"][0]
+    wr = mi.WORKLOADS["redundant_t1024"]
+    assert wr.n_slots == rows["redundant_slots"][0]
+    assert wr.n_slots // wr.n_blocks == rows["slots_per_rank_redundant"][0]
+    assert (wr.n_slots - wr.n_experts) * per_expert == rows["redundant_bytes_fp16"][0]
+    assert w.n_experts // w.n_blocks == rows["experts_per_rank"][0]
+
+
+# ------------------------------------------------------------------ FFN and layer math
+
+
+def test_swiglu_row_matches_torch_float64():
+    H, I = 48, 40
+    x = _bf16((H,), 1.0, 11, 1)
+    g = _bf16((I, H), H ** -0.5, 11, 3)
+    u = _bf16((I, H), H ** -0.5, 11, 4)
+    d = _bf16((H, I), I ** -0.5, 11, 5)
+    got = oracle.swiglu_row(x, g, u, d)
+    ref = _swiglu_torch(_f64(x), _f64(g), _f64(u), _f64(d)).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def _dense_bruteforce(w, x, wr, bias, wg, wu, wd, sg, su, sd):
+    """Every expert on every token, masked by the top-k set (no permutation)."""
+    xf = _f64(x)
+    logits = xf @ _f64(wr).T
+    if bias is not None:
+        logits = logits + torch.from_numpy(bias.astype(np.float64))
+    p = torch.softmax(logits, dim=-1)
+    top = torch.topk(logits, w.top_k, dim=-1).indices
+    mask = torch.zeros_like(p).scatter_(1, top, 1.0)
+    out = torch.zeros(w.tokens, w.hidden, dtype=torch.float64)
+    for e in range(w.n_experts):
+        y = _swiglu_torch(xf, _f64(wg[e]), _f64(wu[e]), _f64(wd[e]))
+        out += (mask[:, e] * p[:, e])[:, None] * y
+    for j in range(w.n_shared):
+        out += _swiglu_torch(xf, _f64(sg[j]), _f64(su[j]), _f64(sd[j]))
+    return out.numpy(), top.numpy()
+
+
+@pytest.mark.parametrize("variant", ["tiny", "tiny_bias", "tiny_k3_2shared"])
+def test_layer_matches_dense_bruteforce(variant):
+    w = mi.WORKLOADS["tiny"]
+    bias = None
+    if variant == "tiny_bias":
+        bias = np.array([0.5, -0.25, 0.0, 1.0, -1.0, 0.25, 0.0, 0.125], dtype=np.float32)
+    if variant == "tiny_k3_2shared":
+        w = w.with_(top_k=3, n_shared=2, inter_shared=24, tokens=21)
+    args = _tiny_inputs(w, bias=bias)
+    r = oracle.moe_forward(w, *args[:3], None, *args[3:])
+    ref, top = _dense_bruteforce(w, *args)
+    assert r["invalid"] == 0
+    assert np.array_equal(np.sort(r["idx"], 1), np.sort(top, 1))
+    np.testing.assert_allclose(r["out"], ref, rtol=1e-11, atol=1e-12 * np.abs(ref).max())
+
+
+def test_identical_experts_give_weight_sum_times_one_ffn():
+    w = _tiny(tokens=12)
+    x, wr, _, wg, wu, wd, sg, su, sd = _tiny_inputs(w)
+    wg[:] = wg[0]
+    wu[:] = wu[0]
+    wd[:] = wd[0]
+    r = oracle.moe_forward(w, x, wr, None, None, wg, wu, wd, sg, su, sd)
+    ysh = oracle.shared_rows(w, x, sg, su, sd)
+    for t in range(w.tokens):
+        ffn = oracle.swiglu_row(x[t], wg[0], wu[0], wd[0])
+        np.testing.assert_allclose(r["out"][t], r["weight"][t].sum() * ffn + ysh[t], rtol=1e-12,
+                                   atol=1e-14)
+
+
+def test_single_expert_top1_is_a_plain_swiglu_mlp():
+    w = _tiny(n_experts=1, n_slots=1, n_blocks=1, top_k=1, tokens=9)
+    x, wr, _, wg, wu, wd, sg, su, sd = _tiny_inputs(w)
+    r = oracle.moe_forward(w, x, wr, None, None, wg, wu, wd, sg, su, sd)
+    assert np.all(r["weight"] == 1.0) and np.all(r["idx"] == 0)
+    xf = _f64(x)
+    ref = _swiglu_torch(xf, _f64(wg[0]), _f64(wu[0]), _f64(wd[0])) + \
+        _swiglu_torch(xf, _f64(sg[0]), _f64(su[0]), _f64(sd[0]))
+    np.testing.assert_allclose(r["out"], ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_routed_part_is_linear_in_down_projection():
+    w = _tiny(tokens=10)
+    x, wr, _, wg, wu, wd, sg, su, sd = _tiny_inputs(w)
+    r1 = oracle.moe_forward(w, x, wr, None, None, wg, wu, wd, sg, su, sd)
+    r2 = oracle.moe_forward(w, x, wr, None, None, wg, wu, (wd.float() * 2).to(torch.bfloat16), sg, su, sd)
+    ysh = oracle.shared_rows(w, x, sg, su, sd)
+    np.testing.assert_allclose(r2["out"] - ysh, 2.0 * (r1["out"] - ysh), rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------------------------------ redundant experts
+
+
+def _replica_tiny():
+    # 8 experts on 4 blocks of 2, one replica slot per block (12 slots)
+    base = _tiny(tokens=40, n_blocks=4, n_slots=8)
+    rep_w = base.with_(n_slots=12)
+    return base, rep_w
+
+
+def test_replica_plan_rule_on_hand_worked_counts():
+    _, w = _replica_tiny()
+    counts = np.array([10, 1, 7, 0, 3, 3, 9, 2], dtype=np.int32)
+    rep = oracle.plan_replicas(w, counts, 3)
+    # hot: 0 (10), 6 (9), 2 (7).  Loads x2 with hot halved:
+    #   block0 = 10 + 2 = 12, block1 = 7 + 0 = 7, block2 = 6 + 6 = 12, block3 = 9 + 4 = 13.
+    # expert 0 (home 0): min over {1,2,3} -> block1 (7) -> slot 1*3+2 = 5; block1 += 10 -> 17
+    # expert 6 (home 3): min over {0,2} (block1 used) -> 12 vs 12, lower -> block0 -> slot 2; -> 21
+    # expert 2 (home 1): min over {2,3} -> block2 (12) -> slot 8
+    assert list(rep) == [5, -1, 8, -1, -1, -1, 2, -1]
+
+
+def test_replica_plan_falls_back_to_home_block():
+    _, w = _replica_tiny()
+    counts = np.array([5, 6, 7, 8, 1, 2, 3, 4], dtype=np.int32)
+    rep = oracle.plan_replicas(w, counts, 4)
+    placed = sorted(int(s) for s in rep if s >= 0)
+    assert placed == [2, 5, 8, 11]  # every block's replica slot used once
+    with pytest.raises(ValueError):
+        oracle.plan_replicas(w, counts, 5)
+    # two blocks, both hot experts in block 0: the second replica can only go home
+    w2 = _tiny(n_experts=4, n_blocks=2, n_slots=6)
+    rep = oracle.plan_replicas(w2, np.array([5, 4, 1, 1], dtype=np.int32), 2)
+    assert list(rep) == [5, 2, -1, -1]
+
+
+def test_replicated_layer_equals_plain_layer_exactly():
+    base, w = _replica_tiny()
+    x = mi.hidden_states(base)
+    wr = mi.router_weight(base)
+    bias = np.array([1.0, 0.0, 0.8, 0.0, 0.0, 0.0, 0.9, 0.0], dtype=np.float32)
+    sg, su, sd = mi.stacked_shared_weights(base)
+    wg0, wu0, wd0 = mi.stacked_expert_weights(base)
+    r0 = oracle.moe_forward(base, x, wr, bias, None, wg0, wu0, wd0, sg, su, sd)
+    expert_counts = np.bincount(r0["idx"].ravel(), minlength=base.n_experts)
+    rep = oracle.plan_replicas(w, expert_counts, 4)
+    wg1, wu1, wd1 = mi.stacked_expert_weights(w, rep)
+    r1 = oracle.moe_forward(w, x, wr, bias, rep, wg1, wu1, wd1, sg, su, sd)
+    assert np.array_equal(r0["out"], r1["out"])  # bit-identical in fp64
+    assert np.array_equal(r0["idx"], r1["idx"])
+    for e in range(base.n_experts):
+        home = oracle.home_slot(w, e)
+        c = r1["counts"][home] + (r1["counts"][rep[e]] if rep[e] >= 0 else 0)
+        assert c == expert_counts[e]
+        if rep[e] >= 0:
+            # odd tokens use the replica
+            odd = sum(1 for t in range(base.tokens) for j in range(base.top_k)
+                      if r0["idx"][t, j] == e and t % 2 == 1)
+            assert r1["counts"][rep[e]] == odd
+    assert r1["counts"].sum() == base.tokens * base.top_k
+
+
+def test_token_output_matches_whole_layer():
+    w = mi.WORKLOADS["tiny"]
+    x, wr, _, wg, wu, wd, sg, su, sd = _tiny_inputs(w)
+    r = oracle.moe_forward(w, x, wr, None, None, wg, wu, wd, sg, su, sd)
+    for t in (0, 7, 15):
+        gud = [(wg[e], wu[e], wd[e]) for e in r["idx"][t]]
+        y = oracle.token_output(w, x[t], r["weight"][t], gud, sg, su, sd)
+        np.testing.assert_allclose(y, r["out"][t], rtol=1e-13, atol=1e-15)
