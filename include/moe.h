@@ -1,0 +1,228 @@
+/*
+ * libmoe — forward pass of a DeepSeek-V3-style Mixture-of-Experts layer on one
+ * GB300 GPU (sm_103a), as a C ABI.
+ *
+ * The layer is the expert-parallel MoE layer of the blog post "专家并行(EP)"
+ * (expert parallelism).  Its section 2.2 follows one token through five steps:
+ *   1. router linear [hidden, n_experts] -> logits -> top-k experts;
+ *   2. dispatch: the token's hidden state goes to each selected expert;
+ *   3. each expert computes its FFN on the rows it received;
+ *   4. combine: the expert outputs return to the token;
+ *   5. output = sum over the top-k of softmax(logits)[i] * expert_output[i]
+ *      plus the shared expert output.
+ * Section 2.1 lays the routed experts out in contiguous blocks (one per EP
+ * rank) with the shared experts replicated; section 6.2 monitors per-expert
+ * arrivals and per-rank load; section 6.3 adds redundant expert slots.
+ * On one device the two all-to-alls become permutations in device memory:
+ * the dispatch buffer holds the rows of every slot contiguously, slot after
+ * slot, so the rows of each EP block are contiguous too.
+ *
+ * Conventions (all entry points)
+ *   - "bf16" arrays are raw 16-bit bfloat16 values (passed as void*).
+ *   - Device pointers are owned by the caller; the library never allocates,
+ *     frees or retains them.  Unless stated otherwise every pointer is a
+ *     device pointer, 16-byte aligned, row-major and densely packed.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device
+ *     work is enqueued asynchronously on it; the call returns once enqueued.
+ *   - Every call returns an int status (MOE_OK = 0).  Nothing aborts, traps
+ *     or prints.  Arguments are validated before anything is enqueued; on an
+ *     error nothing is enqueued and moe_last_error_string() says why.
+ *   - Errors found on the device (an expert id outside [0, E), a bounded
+ *     wait that expired) set a device status word instead of faulting;
+ *     moe_check_status() synchronises the stream, reads and clears it.
+ *   - T = 0 is valid and enqueues nothing.
+ *
+ * Notation: T tokens, H hidden, I routed intermediate, E routed experts,
+ * k top-k, S slots (E, or E + redundant replicas), B blocks (EP ranks),
+ * n_sh shared experts of intermediate I_sh.  Slot layout: block b owns slots
+ * [b*S/B, (b+1)*S/B); its experts b*E/B .. (b+1)*E/B-1 sit in its first E/B
+ * slots in order (home slots), its remaining slots hold replicas.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1     /* null/misaligned pointer, bad size, inconsistent shape */
+#define MOE_ERR_UNSUPPORTED 2     /* valid shape outside this build's kernel limits */
+#define MOE_ERR_CUDA 3            /* a CUDA runtime call or launch failed */
+#define MOE_ERR_DEVICE_TIMEOUT 4  /* a kernel's bounded wait expired (moe_check_status) */
+#define MOE_ERR_DEVICE_STATUS 5   /* a kernel flagged invalid data, e.g. expert id out of range */
+#define MOE_ERR_WORKSPACE 6       /* workspace null or smaller than the *_workspace_size() answer */
+
+/* Expert FFN kernel variant: token chunk of 32 rows (decode: weights streamed
+ * once per 32 rows of an expert) or 256 rows (prefill).  AUTO picks 32 when
+ * T <= 32, else 256.  Results are identical up to fp32 summation order. */
+#define MOE_FFN_AUTO 0
+#define MOE_FFN_DECODE 1
+#define MOE_FFN_PREFILL 2
+
+/* Layer shape.  Limits of this build: 1 <= k <= min(E, 32); E <= 1024;
+ * S <= 1024; E and S divisible by B with S/B >= E/B; H, I, I_sh multiples of 8. */
+typedef struct {
+    int32_t hidden;        /* H */
+    int32_t inter;         /* I */
+    int32_t n_experts;     /* E */
+    int32_t top_k;         /* k */
+    int32_t n_shared;      /* n_sh (0 = no shared expert) */
+    int32_t inter_shared;  /* I_sh */
+    int32_t n_slots;       /* S */
+    int32_t n_blocks;      /* B */
+} moe_shape_t;
+
+/* Text of the last error raised on the calling thread ("" if none). */
+MOE_API const char* moe_last_error_string(void);
+
+/* Library ABI version (increments on any signature change). */
+MOE_API int moe_abi_version(void);
+
+/* Synchronise `stream`, read and clear the current device's status word.
+ * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT or MOE_ERR_DEVICE_STATUS. */
+MOE_API int moe_check_status(void* stream);
+
+/* Bound (nanoseconds of device time) of every spin wait in later launches on
+ * any device; default 2e9.  Returns MOE_ERR_INVALID_ARG for 0. */
+MOE_API int moe_set_wait_limit_ns(uint64_t ns);
+
+/* Launch one kernel whose bounded wait is on a barrier nothing completes: it
+ * gives up after the current wait limit and sets the timeout status, which
+ * moe_check_status() then reports.  For tests of the failure path only. */
+MOE_API int moe_debug_expire_wait(void* stream);
+
+/* ---------------------------------------------------------------- step 1: route
+ * "专家并行(EP)" section 2.2 step 1 (router linear, top-k) and step 5 (the
+ * combine weight softmax(logits)[i]).
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h] (+ bias[e]), fp32 accumulation
+ *     on the tensor cores (router GEMM split over K, partials summed in a fixed
+ *     order);
+ *   topk_idx[t,0..k-1]: the k largest logits, descending, equal values ->
+ *     lower expert index first;
+ *   topk_w[t,j] = softmax over all E logits at topk_idx[t,j] (fp32, not
+ *     renormalised over the top-k).
+ * x [T,H] bf16; w_router [E,H] bf16 (one row per expert); bias [E] fp32 or
+ * NULL.  logits_in [T,E] fp32 or NULL: when given, the GEMM is skipped and the
+ * selection runs on these final logits (bias must then be NULL; x, w_router
+ * may be NULL).  logits_out [T,E] fp32 or NULL receives the logits used.
+ * Outputs topk_idx [T,k] int32, topk_w [T,k] fp32.  ws: device workspace of
+ * at least moe_route_workspace_size() bytes (may be NULL if that is 0). */
+MOE_API size_t moe_route_workspace_size(const moe_shape_t* shape, int T);
+MOE_API int moe_route(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
+              const float* logits_in, float* logits_out, int32_t* topk_idx, float* topk_w, void* ws,
+              size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- EPLB monitor
+ * "专家并行(EP)" section 6.2 ("monitor": tokens arriving at each expert; a
+ * rank's load = sum over its experts) for one batch, and section 6.3 (a token
+ * may use any replica of its expert).
+ *   slot(t,j) = replica_of[e] if replica_of != NULL, replica_of[e] >= 0 and t
+ *               is odd; else e's home slot  (e = topk_idx[t,j]);
+ *   counts[s] = number of assignments to slot s (s < S); counts[S] = number of
+ *               expert ids outside [0,E) (these also set the device status);
+ *   block_counts[b] = sum of counts over block b's slots (NULL to skip).
+ * topk_idx [T,k] int32; replica_of [E] int32 or NULL (values -1 or a slot in
+ * [0,S)); counts [S+1] int32; block_counts [B] int32. */
+MOE_API int moe_expert_histogram(const moe_shape_t* shape, int T, const int32_t* topk_idx, const int32_t* replica_of,
+                         int32_t* counts, int32_t* block_counts, void* stream);
+
+/* Imbalance of per-block loads (host arrays): max / mean, 0 if all are zero.
+ * Section 6.2 rebalances when it exceeds a threshold (typically 1.2). */
+MOE_API double moe_eplb_imbalance(const int32_t* host_block_counts, int n_blocks);
+
+/* Redundant-expert placement (host-only, section 6.2 "copy the overloaded
+ * rank's hottest experts to an idle rank", section 6.3 "8 redundant experts").
+ * From per-expert counts host_expert_counts[E]: the n_rep hottest experts
+ * (count descending, ties -> lower id) each get one replica.  A block's load
+ * starts as the sum of its experts' counts with a hot expert's count halved;
+ * in hot order, each replica goes to the least-loaded block (ties -> lower
+ * block) that has a free replica slot and is not the expert's home block,
+ * else to its home block if that has one free; the block's load then grows by
+ * half the expert's count, and the replica takes that block's first free
+ * replica slot.  Output host_replica_of[E]: slot or -1.
+ * The caller copies the source expert's weights into each replica slot. */
+MOE_API int moe_eplb_plan_replicas(const moe_shape_t* shape, const int32_t* host_expert_counts, int n_rep,
+                           int32_t* host_replica_of);
+
+/* ---------------------------------------------------------------- step 2: dispatch
+ * Section 2.2 step 2.  Slot map and histogram as moe_expert_histogram, then
+ *   offsets[s] = sum_{s'<s} counts[s'] for s <= S+1 (offsets[S+1] = T*k; the
+ *     rows of out-of-range ids sit in [offsets[S], offsets[S+1]));
+ *   rows of slot s: [offsets[s], offsets[s+1]), in ascending a = t*k + j;
+ *   perm[row] = a, inv_perm[a] = row;
+ *   x_disp[row,:] = x[perm[row] / k, :]  (16-byte vector copies).
+ * The buffer is exactly T*k*H*2 bytes; with the equally sized combine payload
+ * that is 2*k*H*2 bytes per token (229,376 B at k=8, H=7168, section 2.3).
+ * x [T,H] bf16; topk_idx [T,k]; replica_of [E] or NULL; outputs slot_of [T*k],
+ * counts [S+1], block_counts [B] (or NULL), offsets [S+2], perm [T*k],
+ * inv_perm [T*k] int32, x_disp [T*k,H] bf16. */
+MOE_API int moe_dispatch(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
+                 const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
+                 int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* x_disp, void* stream);
+
+/* ---------------------------------------------------------------- step 3: expert FFN
+ * Section 2.2 step 3 (each expert's FFN on its rows) with the SwiGLU form
+ * h = silu(X W_g^T) * (X W_u^T), y = h W_d^T; the shared experts (section 2.1)
+ * run on all T rows of x.  Grouped tcgen05 GEMMs, fp32 accumulation, h rounded
+ * to bf16.
+ * moe_expert_gate_up:
+ *   h_disp[row, :] = silu(x_disp[row] . W_g[s]^T) * (x_disp[row] . W_u[s]^T),
+ *     rows of slot s = [offsets[s], offsets[s+1]);
+ *   h_shared[t, j*I_sh + :] = the same with shared expert j on x[t].
+ * moe_expert_down:
+ *   y_disp[row, :] = bf16(h_disp[row] . W_d[s]^T);
+ *   y_shared[t, :] = sum_j h_shared[t, j*I_sh:(j+1)*I_sh] . Ws_d[j]^T (fp32).
+ * moe_expert_ffn = gate_up then down, h in the workspace.
+ * Layouts: w_gate, w_up [S,I,H]; w_down [S,H,I]; ws_gate, ws_up [n_sh,I_sh,H];
+ * ws_down [n_sh,H,I_sh] (bf16, one nn.Linear [out,in] matrix per slot).
+ * x [T,H]; x_disp, y_disp [T*k,H]; h_disp [T*k,I]; h_shared [T,n_sh*I_sh] bf16;
+ * y_shared [T,H] fp32; offsets [S+2] from moe_dispatch.  Shared pointers may be
+ * NULL when n_sh = 0.  Rows of out-of-range ids are not computed. */
+MOE_API int moe_expert_gate_up(const moe_shape_t* shape, int T, const void* x, const void* x_disp,
+                       const int32_t* offsets, const void* w_gate, const void* w_up, const void* ws_gate,
+                       const void* ws_up, void* h_disp, void* h_shared, int mode, void* stream);
+MOE_API int moe_expert_down(const moe_shape_t* shape, int T, const void* h_disp, const void* h_shared,
+                    const int32_t* offsets, const void* w_down, const void* ws_down, void* y_disp,
+                    float* y_shared, int mode, void* stream);
+MOE_API size_t moe_ffn_workspace_size(const moe_shape_t* shape, int T);
+MOE_API int moe_expert_ffn(const moe_shape_t* shape, int T, const void* x, const void* x_disp, const int32_t* offsets,
+                   const void* w_gate, const void* w_up, const void* w_down, const void* ws_gate,
+                   const void* ws_up, const void* ws_down, void* y_disp, float* y_shared, int mode, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- steps 4-5: combine
+ * Section 2.2 steps 4-5 (shared expert gate taken as 1):
+ *   out[t,:] = bf16( sum_{j<k} topk_w[t,j] * y_disp[inv_perm[t*k+j], :] + y_shared[t,:] ),
+ * fp32 accumulation in ascending j, then the shared term.  y_disp [T*k,H] bf16;
+ * inv_perm [T*k]; topk_w [T,k] fp32; y_shared [T,H] fp32 or NULL; out [T,H] bf16. */
+MOE_API int moe_combine(const moe_shape_t* shape, int T, const void* y_disp, const int32_t* inv_perm,
+                const float* topk_w, const float* y_shared, void* out, void* stream);
+
+/* ---------------------------------------------------------------- whole layer
+ * moe_route (from x), moe_dispatch, moe_expert_ffn, moe_combine on one stream
+ * (7 kernel launches; capturable in a CUDA graph).  Intermediates live in the
+ * workspace (moe_workspace_size() bytes).  Optional outputs (NULL to skip):
+ * topk_idx_out [T,k], topk_w_out [T,k], counts_out [S+1], block_counts_out [B].
+ * out [T,H] bf16. */
+MOE_API size_t moe_workspace_size(const moe_shape_t* shape, int T);
+MOE_API int moe_forward(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
+                const int32_t* replica_of, const void* w_gate, const void* w_up, const void* w_down,
+                const void* ws_gate, const void* ws_up, const void* ws_down, void* out, int32_t* topk_idx_out,
+                float* topk_w_out, int32_t* counts_out, int32_t* block_counts_out, int mode, void* ws,
+                size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,232 @@
+"""Python binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function here has the name of a C entry point and forwards torch
+tensors (device memory owned by the caller) as raw pointers, plus the current
+torch CUDA stream.  Every step of the MoE layer runs in libmoe's CUDA
+kernels; there is no fallback path: if libmoe.so is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_DEVICE_TIMEOUT = 4
+MOE_ERR_DEVICE_STATUS = 5
+MOE_ERR_WORKSPACE = 6
+
+MOE_FFN_AUTO = 0
+MOE_FFN_DECODE = 1
+MOE_FFN_PREFILL = 2
+
+# every symbol include/moe.h declares
+EXPORTS = (
+    "moe_last_error_string", "moe_abi_version", "moe_check_status", "moe_set_wait_limit_ns",
+    "moe_debug_expire_wait", "moe_route_workspace_size", "moe_route", "moe_expert_histogram",
+    "moe_eplb_imbalance", "moe_eplb_plan_replicas", "moe_dispatch", "moe_expert_gate_up",
+    "moe_expert_down", "moe_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
+    "moe_workspace_size", "moe_forward",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libmoe error {code}: {msg}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "hidden", "inter", "n_experts", "top_k", "n_shared", "inter_shared", "n_slots", "n_blocks")]
+
+    @classmethod
+    def of(cls, w) -> "Shape":
+        """From any object with those attributes (e.g. a moe_inputs.Workload)."""
+        return cls(w.hidden, w.inter, w.n_experts, w.top_k, w.n_shared, w.inter_shared, w.n_slots, w.n_blocks)
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+_SIG = {
+    "moe_last_error_string": (ctypes.c_char_p, []),
+    "moe_abi_version": (_I, []),
+    "moe_check_status": (_I, [_P]),
+    "moe_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
+    "moe_debug_expire_wait": (_I, [_P]),
+    "moe_route_workspace_size": (_Z, [_P, _I]),
+    "moe_route": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_histogram": (_I, [_P, _I, _P, _P, _P, _P, _P]),
+    "moe_eplb_imbalance": (ctypes.c_double, [_P, _I]),
+    "moe_eplb_plan_replicas": (_I, [_P, _P, _I, _P]),
+    "moe_dispatch": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_expert_gate_up": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "moe_expert_down": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
+    "moe_ffn_workspace_size": (_Z, [_P, _I]),
+    "moe_expert_ffn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
+    "moe_combine": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_workspace_size": (_Z, [_P, _I]),
+    "moe_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
+}
+
+
+def build_library(force: bool = False) -> str:
+    """Compile libmoe.so in-tree (nvcc, sm_103a)."""
+    import importlib
+    return importlib.import_module(__name__ + ".build").build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmoe.so not built ({LIB_PATH}); run moe_expert_layer_06_gb300.build_library()")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIG.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def last_error() -> str:
+    return lib().moe_last_error_string().decode()
+
+
+def _check(code: int):
+    if code != MOE_OK:
+        raise MoeError(code, last_error())
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, torch.Tensor):
+        if t.numel() and not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+        return t.data_ptr() if t.numel() else None
+    raise TypeError(type(t))
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _shape(shape):
+    return ctypes.byref(shape if isinstance(shape, Shape) else Shape.of(shape))
+
+
+# ------------------------------------------------------------------ entry points
+
+def moe_check_status(stream=None) -> int:
+    return lib().moe_check_status(_stream(stream))
+
+
+def moe_set_wait_limit_ns(ns: int):
+    _check(lib().moe_set_wait_limit_ns(int(ns)))
+
+
+def moe_debug_expire_wait(stream=None):
+    _check(lib().moe_debug_expire_wait(_stream(stream)))
+
+
+def moe_route_workspace_size(shape, T: int) -> int:
+    return lib().moe_route_workspace_size(_shape(shape), T)
+
+
+def moe_route(shape, T, x, w_router, bias, logits_in, logits_out, topk_idx, topk_w, ws, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(lib().moe_route(_shape(shape), T, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(logits_in),
+                           _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_expert_histogram(shape, T, topk_idx, replica_of, counts, block_counts, stream=None):
+    _check(lib().moe_expert_histogram(_shape(shape), T, _ptr(topk_idx), _ptr(replica_of), _ptr(counts),
+                                      _ptr(block_counts), _stream(stream)))
+
+
+def moe_eplb_imbalance(block_counts) -> float:
+    import numpy as np
+    a = np.ascontiguousarray(block_counts, dtype=np.int32)
+    return lib().moe_eplb_imbalance(a.ctypes.data, a.size)
+
+
+def moe_eplb_plan_replicas(shape, expert_counts, n_rep: int):
+    import numpy as np
+    c = np.ascontiguousarray(expert_counts, dtype=np.int32)
+    out = np.empty(shape.n_experts, dtype=np.int32)
+    _check(lib().moe_eplb_plan_replicas(_shape(shape), c.ctypes.data, n_rep, out.ctypes.data))
+    return out
+
+
+def moe_dispatch(shape, T, x, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm,
+                 x_disp, stream=None):
+    _check(lib().moe_dispatch(_shape(shape), T, _ptr(x), _ptr(topk_idx), _ptr(replica_of), _ptr(slot_of),
+                              _ptr(counts), _ptr(block_counts), _ptr(offsets), _ptr(perm), _ptr(inv_perm),
+                              _ptr(x_disp), _stream(stream)))
+
+
+def moe_expert_gate_up(shape, T, x, x_disp, offsets, w_gate, w_up, ws_gate, ws_up, h_disp, h_shared,
+                       mode=MOE_FFN_AUTO, stream=None):
+    _check(lib().moe_expert_gate_up(_shape(shape), T, _ptr(x), _ptr(x_disp), _ptr(offsets), _ptr(w_gate),
+                                    _ptr(w_up), _ptr(ws_gate), _ptr(ws_up), _ptr(h_disp), _ptr(h_shared), mode,
+                                    _stream(stream)))
+
+
+def moe_expert_down(shape, T, h_disp, h_shared, offsets, w_down, ws_down, y_disp, y_shared,
+                    mode=MOE_FFN_AUTO, stream=None):
+    _check(lib().moe_expert_down(_shape(shape), T, _ptr(h_disp), _ptr(h_shared), _ptr(offsets), _ptr(w_down),
+                                 _ptr(ws_down), _ptr(y_disp), _ptr(y_shared), mode, _stream(stream)))
+
+
+def moe_ffn_workspace_size(shape, T: int) -> int:
+    return lib().moe_ffn_workspace_size(_shape(shape), T)
+
+
+def moe_expert_ffn(shape, T, x, x_disp, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_disp,
+                   y_shared, mode, ws, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(lib().moe_expert_ffn(_shape(shape), T, _ptr(x), _ptr(x_disp), _ptr(offsets), _ptr(w_gate),
+                                _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
+                                _ptr(y_disp), _ptr(y_shared), mode, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_combine(shape, T, y_disp, inv_perm, topk_w, y_shared, out, stream=None):
+    _check(lib().moe_combine(_shape(shape), T, _ptr(y_disp), _ptr(inv_perm), _ptr(topk_w), _ptr(y_shared),
+                             _ptr(out), _stream(stream)))
+
+
+def moe_workspace_size(shape, T: int) -> int:
+    return lib().moe_workspace_size(_shape(shape), T)
+
+
+def moe_forward(shape, T, x, w_router, bias, replica_of, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, out,
+                topk_idx_out=None, topk_w_out=None, counts_out=None, block_counts_out=None,
+                mode=MOE_FFN_AUTO, ws=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(lib().moe_forward(_shape(shape), T, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(replica_of),
+                             _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
+                             _ptr(out), _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out),
+                             _ptr(block_counts_out), mode, _ptr(ws), ws_bytes, _stream(stream)))

@@ -1,0 +1,80 @@
+// Combine of the MoE layer on one device, fused with the shared-expert add.
+//
+// Blog post "专家并行(EP)", section 2.2 steps 4-5: expert outputs return to
+// their token (here: a gather through inv_perm) and
+//   out[t] = sum_{j<k} softmax(logits)[idx_j] * expert_out_j + shared_out[t],
+// accumulated in fp32 in ascending j, then the shared expert output, rounded
+// once to bf16.  8 bf16 (16 bytes) per thread per step.
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y_disp,
+                                                      const int32_t* __restrict__ inv_perm,
+                                                      const float* __restrict__ topk_w,
+                                                      const float4* __restrict__ y_shared, int T, int k,
+                                                      int vec_per_row, uint4* __restrict__ out) {
+    const size_t total = (size_t)T * vec_per_row;
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(idx / vec_per_row);
+        const int c = (int)(idx - (size_t)t * vec_per_row);
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int row = __ldg(inv_perm + (size_t)t * k + j);
+            const float w = __ldg(topk_w + (size_t)t * k + j);
+            float y[8];
+            unpack8(__ldg(y_disp + (size_t)row * vec_per_row + c), y);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, y[i], acc[i]);
+        }
+        if (y_shared) {
+            const float4 s0 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2);
+            const float4 s1 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2 + 1);
+            acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
+            acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
+        }
+        uint4 o;
+        o.x = pack2(acc[0], acc[1]);
+        o.y = pack2(acc[2], acc[3]);
+        o.z = pack2(acc[4], acc[5]);
+        o.w = pack2(acc[6], acc[7]);
+        out[idx] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y_disp, const int32_t* inv_perm, const float* topk_w,
+                           const float* y_shared, int T, int k, int hidden, uint16_t* out,
+                           cudaStream_t stream) {
+    const int vpr = hidden / 8;
+    const size_t total = (size_t)T * vpr;
+    if (total == 0) return cudaSuccess;
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = (size_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    combine_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(y_disp), inv_perm, topk_w,
+                                                         reinterpret_cast<const float4*>(y_shared), T, k, vpr,
+                                                         reinterpret_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

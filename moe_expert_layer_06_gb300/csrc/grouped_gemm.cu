@@ -1,0 +1,469 @@
+// Grouped swap-AB GEMM on the 5th-generation tensor cores (tcgen05 + TMEM),
+// fed by TMA: the expert FFN of the MoE layer (gate/up + SwiGLU, and down) and
+// the router linear.
+//
+// Expert-parallel layer of the blog post "专家并行(EP)", section 2.2, step 3:
+// every expert computes its FFN on the token rows dispatched to it.  The
+// weights are the large operand (88 MB per expert; a decode step touches
+// ~160 experts), tokens the small one (a few to a few hundred rows per
+// expert).  So the weight matrix is the UMMA "A" operand (M = 128 output
+// rows per tile) and the expert's token rows the "B" operand (N = up to BN
+// rows, rounded up to 16): each weight tile streams from HBM once per token
+// chunk, and with BN = 256 each expert's weights are read exactly once up to
+// 256 rows per expert.
+//
+// Work item = (matrix, 128-row block of outputs, token chunk[, K split]).
+// The item list is derived on the device from the dispatch offsets, so no
+// host synchronisation is needed.  A persistent CTA per SM takes items
+// round-robin; warp roles:
+//   warp 0      TMA producer (one elected lane)   smem ring of STAGES stages
+//   warp 1      MMA issuer   (one elected lane)   TMEM accumulators (x2 when they fit)
+//   warps 2..9  epilogue: tcgen05.ld -> SwiGLU / convert -> global stores
+// Every mbarrier wait is bounded; on expiry the kernel raises the status word,
+// drains its own copies and MMAs (bounded) and frees its TMEM.
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 320;        // 10 warps
+constexpr int kEpiWarps = 8;
+constexpr int kABytes = 128 * 64 * 2;  // one 128x64 bf16 weight tile
+constexpr int kMaxSlots = 1024;
+
+struct Item {
+    int shared;  // 0: routed or router, 1: shared expert
+    int z;       // slot | shared expert | 0
+    int m0;      // first output row of the A tile
+    int row0;    // first B row
+    int nrows;   // valid B rows (<= BN)
+    int kc0, kc1;
+    int ks;      // router K split
+};
+
+template <int MODE>
+struct Traits {
+    static constexpr int NA = (MODE == kGateUp) ? 2 : 1;
+};
+
+__host__ __device__ constexpr int pow2_at_least(int v) {
+    int p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+template <int MODE, int BN, int STAGES>
+struct Config {
+    static constexpr int NA = Traits<MODE>::NA;
+    static constexpr int kBBytes = BN * 64 * 2;
+    static constexpr int kStageBytes = NA * kABytes + kBBytes;
+    static constexpr int kAccCols = NA * BN;
+    static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = pow2_at_least(kNumAcc * kAccCols);
+    static constexpr int kBarBytes = (2 * STAGES + 2 * kNumAcc + 1) * 8;
+    static constexpr int kTableBytes = (3 * kMaxSlots + 8) * 4;
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + 16 + kTableBytes;
+    static_assert(kTmemCols <= 512, "TMEM overflow");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
+};
+
+// Shared-memory tables describing the routed items of this launch.
+struct Table {
+    int* pre;   // [S+1] exclusive prefix of routed items per slot
+    int* cnt;   // [S]   rows per slot
+    int* offs;  // [S]   first dispatch row per slot
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+template <int MODE, int BN>
+__device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Table& tb, int n_sh_items) {
+    Item it;
+    it.ks = 0;
+    if (MODE == kRouter) {
+        const int chunks = cdiv(a.T, BN);
+        it.shared = 0;
+        it.z = 0;
+        it.ks = i % a.ksplit;
+        const int r = i / a.ksplit;
+        const int c = r % chunks;
+        it.m0 = (r / chunks) * 128;
+        it.row0 = c * BN;
+        it.nrows = min(BN, a.T - it.row0);
+        it.kc0 = it.ks * a.kc_split;
+        it.kc1 = min(a.kc_routed, it.kc0 + a.kc_split);
+        return it;
+    }
+    if (i < n_sh_items) {
+        const int chunks = cdiv(a.T, BN);
+        const int mb = cdiv(a.m_shared, 128);
+        it.shared = 1;
+        int r = i;
+        if (MODE == kGateUp) {
+            it.z = r / (mb * chunks);
+            r -= it.z * mb * chunks;
+        } else {
+            it.z = 0;
+        }
+        it.m0 = (r / chunks) * 128;
+        it.row0 = (r % chunks) * BN;
+        it.nrows = min(BN, a.T - it.row0);
+        it.kc0 = 0;
+        it.kc1 = a.kc_shared;
+        return it;
+    }
+    i -= n_sh_items;
+    // slot s: the last slot with pre[s] <= i (pre is non-decreasing)
+    int lo = 0, hi = a.n_slots - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tb.pre[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    const int l = i - tb.pre[s];
+    const int chunks = cdiv(tb.cnt[s], BN);
+    const int c = l % chunks;
+    it.shared = 0;
+    it.z = s;
+    it.m0 = (l / chunks) * 128;
+    it.row0 = tb.offs[s] + c * BN;
+    it.nrows = min(BN, tb.cnt[s] - c * BN);
+    it.kc0 = 0;
+    it.kc1 = a.kc_routed;
+    return it;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int MODE, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs a) {
+    using C = Config<MODE, BN, STAGES>;
+    constexpr int NA = C::NA;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + C::kNumAcc;
+    uint64_t* mma_done = tempty + C::kNumAcc;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* table = reinterpret_cast<int*>(tmem_slot + 4);
+    Table tb{table, table + kMaxSlots + 1, table + 2 * kMaxSlots + 1};
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const unsigned long long limit = a.st.limit_ns;
+
+    // ---- work list: shared items first, then routed items slot by slot
+    int n_sh_items = 0;
+    if (MODE != kRouter && a.n_shared > 0) {
+        const int chunks = cdiv(a.T, BN);
+        const int mb = cdiv(a.m_shared, 128);
+        n_sh_items = (MODE == kGateUp ? a.n_shared : 1) * mb * chunks;
+    }
+    int n_items;
+    if (MODE == kRouter) {
+        n_items = cdiv(a.m_routed, 128) * cdiv(a.T, BN) * a.ksplit;
+    } else {
+        if (warp == 0) {
+            const int S = a.n_slots;
+            const int per = cdiv(S, 32);
+            const int s0 = min(S, lane * per), s1 = min(S, s0 + per);
+            const int mb = cdiv(a.m_routed, 128);
+            int sum = 0;
+            for (int s = s0; s < s1; ++s) {
+                const int o = a.offsets[s];
+                const int c = a.offsets[s + 1] - o;
+                tb.cnt[s] = c;
+                tb.offs[s] = o;
+                sum += cdiv(c, BN) * mb;
+            }
+            int incl = sum;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += v;
+            }
+            int run = incl - sum;
+            for (int s = s0; s < s1; ++s) {
+                tb.pre[s] = run;
+                run += cdiv(tb.cnt[s], BN) * mb;
+            }
+            if (lane == 31) tb.pre[S] = incl;
+        }
+        __syncthreads();
+        n_items = n_sh_items + tb.pre[a.n_slots];
+    }
+    if ((int)blockIdx.x >= n_items) return;  // uniform across the CTA
+
+    // ---- setup: barriers, TMEM
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int s = 0; s < C::kNumAcc; ++s) {
+            mbar_init(smem_u32(&tfull[s]), 1);
+            mbar_init(smem_u32(&tempty[s]), kEpiWarps);
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&a.a0);
+        tma_prefetch_desc(&a.b);
+        if (NA == 2) tma_prefetch_desc(&a.a1);
+        if (MODE != kRouter && a.n_shared > 0) {
+            tma_prefetch_desc(&a.sa0);
+            tma_prefetch_desc(&a.sb);
+            if (NA == 2) tma_prefetch_desc(&a.sa1);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 0) {
+        // =========================== TMA producer ===========================
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_x = policy_evict_last();
+            uint32_t armed[STAGES];
+            for (int s = 0; s < STAGES; ++s) armed[s] = 2;  // 2 = never armed
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+                const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
+                const CUtensorMap* ma0 = it.shared ? &a.sa0 : &a.a0;
+                const CUtensorMap* ma1 = it.shared ? &a.sa1 : &a.a1;
+                const CUtensorMap* mb = it.shared ? &a.sb : &a.b;
+                const int nb = (it.nrows + 15) >> 4;
+                const uint32_t bytes = NA * kABytes + nb * 2048;
+                for (int kc = it.kc0; kc < it.kc1; ++kc) {
+                    if (*abort_flag || !mbar_wait(smem_u32(&empty[stage]), phase ^ 1, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * C::kStageBytes;
+                    uint8_t* sb = sa + NA * kABytes;
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    armed[stage] = phase;
+                    int ka = kc * 64, kb = kc * 64, za = it.z, bmid = 0;
+                    if (MODE == kDown && it.shared) {
+                        za = kc / a.kc_per_sh;
+                        ka = (kc - za * a.kc_per_sh) * 64;
+                        kb = ka;
+                        bmid = za;
+                    }
+                    tma_load_3d(smem_u32(sa), ma0, fb, ka, it.m0, za, pol_w);
+                    if (NA == 2) tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
+                    for (int b = 0; b < nb; ++b)
+                        tma_load_3d(smem_u32(sb + b * 2048), mb, fb, kb, bmid, it.row0 + 16 * b, pol_x);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_status(a.st, kStatusWaitTimeout);
+            }
+            // drain: every copy this thread issued has landed before the CTA exits
+            for (int s = 0; s < STAGES; ++s)
+                if (armed[s] != 2) mbar_wait(smem_u32(&full[s]), armed[s], limit);
+        }
+    } else if (warp == 1) {
+        // =========================== MMA issuer =============================
+        if (lane == 0) {
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+                const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
+                const int nb = (it.nrows + 15) >> 4;
+                const uint32_t idesc = umma_idesc_bf16(128, nb * 16);
+                if (*abort_flag || !mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, limit)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tbase + acc * C::kAccCols;
+                for (int kc = it.kc0; kc < it.kc1; ++kc) {
+                    if (*abort_flag || !mbar_wait(smem_u32(&full[stage]), phase, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+                    const uint64_t adesc0 = umma_desc_sw128(sa);
+                    const uint64_t adesc1 = umma_desc_sw128(sa + kABytes);
+                    const uint64_t bdesc = umma_desc_sw128(sa + NA * kABytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t accum = (kc > it.kc0 || kk > 0) ? 1u : 0u;
+                        umma_bf16(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                        if (NA == 2) umma_bf16(d0 + BN, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                    }
+                    umma_commit(smem_u32(&empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&tfull[acc]));
+                if (++acc == C::kNumAcc) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_status(a.st, kStatusWaitTimeout);
+            }
+            // drain: all MMAs issued by this thread are complete before TMEM is freed
+            umma_commit(smem_u32(mma_done));
+            mbar_wait(smem_u32(mma_done), 0, limit);
+        }
+    } else {
+        // =========================== epilogue ================================
+        const int ew = warp - 2;
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int half = ew >> 2;         // column groups: even (0) or odd (1)
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+            const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
+            const int nb = (it.nrows + 15) >> 4;
+            if (*abort_flag || !mbar_wait(smem_u32(&tfull[acc]), acc_phase, limit)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int mrow = it.m0 + q * 32 + lane;
+            const int mlim = it.shared ? a.m_shared : a.m_routed;
+            const bool row_ok = mrow < mlim;
+            const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + acc * C::kAccCols;
+            for (int g = half; g < nb; g += 2) {
+                float v0[16];
+                tmem_ld16(tl + g * 16, v0);
+                if (MODE == kGateUp) {
+                    float v1[16];
+                    tmem_ld16(tl + BN + g * 16, v1);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        __nv_bfloat16* dst;
+                        int ld;
+                        if (it.shared) {
+                            dst = reinterpret_cast<__nv_bfloat16*>(a.out_sh) + (size_t)it.z * a.sh_col_stride + mrow;
+                            ld = a.out_sh_ld;
+                        } else {
+                            dst = reinterpret_cast<__nv_bfloat16*>(a.out) + mrow;
+                            ld = a.out_ld;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = g * 16 + j;
+                            if (col < it.nrows)
+                                dst[(size_t)(it.row0 + col) * ld] = __float2bfloat16_rn(silu_f(v0[j]) * v1[j]);
+                        }
+                    }
+                } else {
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        if (MODE == kRouter) {
+                            float* dst = reinterpret_cast<float*>(a.out) + (size_t)it.ks * a.T * a.out_ld + mrow;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int col = g * 16 + j;
+                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_ld] = v0[j];
+                            }
+                        } else if (it.shared) {
+                            float* dst = reinterpret_cast<float*>(a.out_sh) + mrow;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int col = g * 16 + j;
+                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_sh_ld] = v0[j];
+                            }
+                        } else {
+                            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) + mrow;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int col = g * 16 + j;
+                                if (col < it.nrows)
+                                    dst[(size_t)(it.row0 + col) * a.out_ld] = __float2bfloat16_rn(v0[j]);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+            if (++acc == C::kNumAcc) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            raise_status(a.st, kStatusWaitTimeout);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+}
+
+template <int MODE, int BN, int STAGES>
+cudaError_t launch_one(const GemmArgs& args, int grid, cudaStream_t stream) {
+    using C = Config<MODE, BN, STAGES>;
+    auto kern = grouped_gemm_kernel<MODE, BN, STAGES>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_max_slots() { return kMaxSlots; }
+
+cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, cudaStream_t stream) {
+    if (grid <= 0) return cudaSuccess;
+    if (bn == 32) {
+        switch (mode) {
+            case kGateUp: return launch_one<kGateUp, 32, 5>(args, grid, stream);
+            case kDown: return launch_one<kDown, 32, 8>(args, grid, stream);
+            case kRouter: return launch_one<kRouter, 32, 8>(args, grid, stream);
+        }
+    } else if (bn == 256) {
+        switch (mode) {
+            case kGateUp: return launch_one<kGateUp, 256, 3>(args, grid, stream);
+            case kDown: return launch_one<kDown, 256, 4>(args, grid, stream);
+            case kRouter: return launch_one<kRouter, 256, 4>(args, grid, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,88 @@
+// Host-side declarations shared by the library's translation units (not part
+// of the public C ABI, which is include/moe.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------- grouped swap-AB GEMM (tcgen05)
+enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2 };
+
+// One launch computes D = A * B^T for a list of work items.  A is a weight
+// tile of 128 output rows (the UMMA M operand), B is a chunk of up to BN
+// token rows (the UMMA N operand), K runs over 64-element chunks.  Every
+// operand is read by TMA through the tensor maps below (3-D, bf16, 128-byte
+// swizzle, box {64, rows, 1}).
+struct GemmArgs {
+    CUtensorMap a0;   // routed weights: gate [S,I,H] | down [S,H,I] | router [1,E,H]
+    CUtensorMap a1;   // routed up weights [S,I,H] (gate/up only)
+    CUtensorMap b;    // routed activations: x_disp [T*k,H] | h_disp [T*k,I] | x [T,H]
+    CUtensorMap sa0;  // shared gate [n_sh,I_sh,H] | shared down [n_sh,H,I_sh]
+    CUtensorMap sa1;  // shared up [n_sh,I_sh,H]
+    CUtensorMap sb;   // shared activations: x [T,H] | h_sh [T,n_sh,I_sh]
+    const int32_t* offsets;  // [S+2] dispatch row offsets (gate/up, down)
+    int n_slots;
+    int T;
+    int m_routed;     // output rows per routed matrix: I | H | E
+    int kc_routed;    // 64-wide K chunks of a routed item
+    int n_shared;     // shared experts (0: none)
+    int m_shared;     // output rows per shared matrix: I_sh | H
+    int kc_shared;    // K chunks of a shared item: ceil(H/64) | n_sh*ceil(I_sh/64)
+    int kc_per_sh;    // down: K chunks per shared expert, ceil(I_sh/64)
+    int ksplit;       // router: number of K splits
+    int kc_split;     // router: K chunks per split
+    void* out;        // h_disp bf16 | y_disp bf16 | logit partials f32 [ksplit,T,E]
+    int out_ld;
+    void* out_sh;     // h_sh bf16 [T, n_sh*I_sh] | y_sh f32 [T,H]
+    int out_sh_ld;
+    int sh_col_stride;  // gate/up: I_sh (column offset of shared expert j in h_sh)
+    DevStatus st;
+};
+
+// Launch the grouped GEMM for `mode` with token chunk bn (32 or 256).
+cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, cudaStream_t stream);
+int gemm_max_slots();
+
+// ---------------------------------------------------------------- TMA tensor maps
+// 3-D bf16 tensor map, dims innermost first (elements), strides of dims 1,2 in bytes.
+int make_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                 uint32_t box2);
+
+// ---------------------------------------------------------------- routing
+cudaError_t launch_topk(const float* partials, int ksplit, const float* bias, int T, int E, int k,
+                        float* logits_out, int32_t* topk_idx, float* topk_w, const DevStatus& st,
+                        cudaStream_t stream);
+
+// ---------------------------------------------------------------- dispatch / histogram
+struct DispatchArgs {
+    int T, k, E, S, n_blocks, hidden;
+    const int32_t* topk_idx;
+    const int32_t* replica_of;
+    int32_t* slot_of;
+    int32_t* counts;        // [S+1]
+    int32_t* block_counts;  // [n_blocks] or null
+    int32_t* offsets;       // [S+2] or null (histogram only)
+    int32_t* perm;          // [T*k] or null
+    int32_t* inv_perm;      // [T*k] or null
+    DevStatus st;
+};
+cudaError_t launch_index_pass(const DispatchArgs& a, cudaStream_t stream);
+cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* perm, int n_rows, int k, int hidden,
+                                uint16_t* x_disp, cudaStream_t stream);
+int dispatch_max_slots();
+
+// ---------------------------------------------------------------- combine
+cudaError_t launch_combine(const uint16_t* y_disp, const int32_t* inv_perm, const float* topk_w,
+                           const float* y_shared, int T, int k, int hidden, uint16_t* out,
+                           cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,116 @@
+"""Helpers shared by the test files: device inputs, tolerance checks, oracle runs."""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+
+import numpy as np
+import torch
+
+import moe_expert_layer_06_gb300 as m
+import moe_inputs as mi
+import oracle
+
+# Float tolerance of the bf16 layer output against the fp64 oracle.
+REL_FROB = 5e-3
+ELEM_RMS = 3e-2
+TOPK_GAP = 1e-4
+
+THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy()
+
+
+def assert_close(got, want, rel_frob=REL_FROB, elem_rms=ELEM_RMS, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = got - want
+    nw = np.linalg.norm(want)
+    rel = np.linalg.norm(err) / nw if nw > 0 else np.linalg.norm(err)
+    rms = np.sqrt(np.mean(want ** 2)) if want.size else 0.0
+    mx = np.abs(err).max() if err.size else 0.0
+    assert rel <= rel_frob, f"{what}: relative Frobenius error {rel:.3e} > {rel_frob}"
+    assert mx <= elem_rms * rms + 1e-30, f"{what}: max |err| {mx:.3e} > {elem_rms}*rms ({rms:.3e})"
+    return rel, mx / rms if rms else 0.0
+
+
+def topk_gap(logits: np.ndarray, k: int) -> np.ndarray:
+    """Gap between the k-th and (k+1)-th largest logit of each row (inf if k = E)."""
+    s = -np.sort(-logits, axis=1)
+    if s.shape[1] <= k:
+        return np.full(s.shape[0], np.inf)
+    return s[:, k - 1] - s[:, k]
+
+
+def parallel_router_logits(w, x_cpu, wr_cpu, bias):
+    """Oracle logits for all rows, rows split across host threads (the C code is pure)."""
+    T = x_cpu.shape[0]
+    chunks = np.array_split(np.arange(T), min(THREADS, max(1, T)))
+    with cf.ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(lambda r: oracle.router_logits(w, x_cpu[r[0]:r[-1] + 1], wr_cpu, bias)
+                            if len(r) else np.zeros((0, w.n_experts)), chunks))
+    return np.concatenate(parts, axis=0)
+
+
+class DeviceLayer:
+    """Device copies of one workload's inputs (generated on the device)."""
+
+    def __init__(self, w, device="cuda", replica_of=None, weights=None):
+        self.w = w
+        self.dev = torch.device(device)
+        self.x = mi.hidden_states(w, device=self.dev)
+        self.wr = mi.router_weight(w, device=self.dev)
+        b = mi.router_bias(w)
+        self.bias = torch.from_numpy(b).to(self.dev) if b is not None else None
+        self.replica_of_np = replica_of
+        self.replica_of = (torch.from_numpy(np.asarray(replica_of, dtype=np.int32)).to(self.dev)
+                           if replica_of is not None else None)
+        if weights is None:
+            weights = mi.stacked_expert_weights(w, replica_of, device=self.dev)
+        self.wg, self.wu, self.wd = weights
+        self.sg, self.su, self.sd = mi.stacked_shared_weights(w, device=self.dev)
+
+    def forward(self, mode=m.MOE_FFN_AUTO):
+        w, T = self.w, self.w.tokens
+        out = torch.empty((T, w.hidden), dtype=torch.bfloat16, device=self.dev)
+        idx = torch.empty((T, w.top_k), dtype=torch.int32, device=self.dev)
+        tw = torch.empty((T, w.top_k), dtype=torch.float32, device=self.dev)
+        counts = torch.empty(w.n_slots + 1, dtype=torch.int32, device=self.dev)
+        blocks = torch.empty(w.n_blocks, dtype=torch.int32, device=self.dev)
+        ws = torch.empty(max(1, m.moe_workspace_size(w, T)), dtype=torch.uint8, device=self.dev)
+        m.moe_forward(w, T, self.x, self.wr, self.bias, self.replica_of, self.wg, self.wu, self.wd,
+                      self.sg, self.su, self.sd, out, idx, tw, counts, blocks, mode=mode, ws=ws)
+        rc = m.moe_check_status()
+        assert rc == 0, m.last_error()
+        return dict(out=out, idx=idx, w=tw, counts=counts, blocks=blocks)
+
+
+def oracle_token_rows(w, tokens, x_cpu, wr_cpu, bias, replica_of=None, expert_cache=None):
+    """Oracle routing and output for a sample of tokens of a full-size workload.
+
+    Only the experts those tokens select are generated (on the CPU).
+    """
+    expert_cache = {} if expert_cache is None else expert_cache
+    xs = x_cpu[tokens]
+    logits = oracle.router_logits(w, xs, wr_cpu, bias)
+    idx, wt = oracle.topk_softmax(logits, w.top_k)
+    need = sorted(set(int(e) for e in idx.ravel()) - set(expert_cache))
+    for e in need:
+        expert_cache[e] = mi.expert_weights(w, e)
+    sg, su, sd = mi.stacked_shared_weights(w)
+
+    def one(i):
+        gud = [expert_cache[int(e)] for e in idx[i]]
+        ys = [oracle.swiglu_row(xs[i], *g) for g in gud]
+        out = oracle.token_output(w, xs[i], wt[i], gud, sg, su, sd)
+        return ys, out
+
+    with cf.ThreadPoolExecutor(min(THREADS, len(tokens))) as ex:
+        res = list(ex.map(one, range(len(tokens))))
+    return dict(logits=logits, idx=idx, weight=wt, y=[r[0] for r in res], out=np.stack([r[1] for r in res]))

@@ -1,0 +1,135 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+validates arguments before touching the device, and its host-only EPLB helpers
+agree with the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import moe_expert_layer_06_gb300 as m
+import moe_inputs as mi
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+FAKE = 0x10000  # 16-byte aligned address that is never dereferenced on the host
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    m.build_library()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"^MOE_API [^(]*?\b(moe_\w+)\(", src, flags=re.M)
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared()
+    assert len(names) >= 18
+    lib = ctypes.CDLL(m.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(m.EXPORTS)
+    assert m.lib().moe_abi_version() == 1
+
+
+def _shape(**kw):
+    return m.Shape.of(mi.WORKLOADS["decode_t32"].with_(**kw))
+
+
+def test_shape_validation_codes():
+    L = m.lib()
+    buf = ctypes.c_void_p(FAKE)
+    assert L.moe_route(None, 4, buf, buf, None, None, None, buf, buf, buf, 1 << 30, None) == m.MOE_ERR_INVALID_ARG
+    assert "shape" in m.last_error()
+    cases = [
+        (dict(top_k=300), m.MOE_ERR_INVALID_ARG),     # k > E
+        (dict(top_k=33, n_experts=64, n_slots=64), m.MOE_ERR_INVALID_ARG),  # k > 32
+        (dict(hidden=7170), m.MOE_ERR_INVALID_ARG),   # H % 8
+        (dict(inter=2050), m.MOE_ERR_INVALID_ARG),
+        (dict(n_slots=260), m.MOE_ERR_INVALID_ARG),   # S % blocks
+        (dict(n_slots=128, n_experts=256), m.MOE_ERR_INVALID_ARG),
+        (dict(n_experts=2048, n_slots=2048), m.MOE_ERR_UNSUPPORTED),
+        (dict(n_slots=1032), m.MOE_ERR_UNSUPPORTED),
+        (dict(n_blocks=0), m.MOE_ERR_INVALID_ARG),
+    ]
+    for kw, code in cases:
+        s = _shape(**kw)
+        rc = L.moe_route(ctypes.byref(s), 4, buf, buf, None, None, None, buf, buf, buf, 1 << 30, None)
+        assert rc == code, (kw, rc, m.last_error())
+    s = _shape()
+    assert L.moe_route(ctypes.byref(s), -1, buf, buf, None, None, None, buf, buf, buf, 0, None) == m.MOE_ERR_INVALID_ARG
+
+
+def test_pointer_and_workspace_validation_codes():
+    L = m.lib()
+    s = _shape()
+    b = ctypes.c_void_p(FAKE)
+    mis = ctypes.c_void_p(FAKE + 2)
+    # null / misaligned
+    assert L.moe_route(ctypes.byref(s), 4, None, b, None, None, None, b, b, b, 1 << 30, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_route(ctypes.byref(s), 4, mis, b, None, None, None, b, b, b, 1 << 30, None) == m.MOE_ERR_INVALID_ARG
+    assert "aligned" in m.last_error()
+    # logits_in together with bias
+    assert L.moe_route(ctypes.byref(s), 4, None, None, b, b, None, b, b, None, 0, None) == m.MOE_ERR_INVALID_ARG
+    # workspace too small
+    need = L.moe_route_workspace_size(ctypes.byref(s), 4)
+    assert need > 0
+    assert L.moe_route(ctypes.byref(s), 4, b, b, None, None, None, b, b, b, need - 1, None) == m.MOE_ERR_WORKSPACE
+    fw = L.moe_workspace_size(ctypes.byref(s), 32)
+    assert fw > 32 * 8 * 7168 * 2 * 2
+    args = [ctypes.byref(s), 32] + [b] * 11 + [None] * 4 + [0, b, fw - 1, None]
+    assert L.moe_forward(*args) == m.MOE_ERR_WORKSPACE
+    args = [ctypes.byref(s), 32] + [b] * 11 + [None] * 4 + [7, b, fw, None]
+    assert L.moe_forward(*args) == m.MOE_ERR_INVALID_ARG  # bad mode
+    assert L.moe_ffn_workspace_size(ctypes.byref(s), 32) == 32 * 8 * 2048 * 2 + 32 * 2 * 2048 * 2
+    # combine: null output
+    assert L.moe_combine(ctypes.byref(s), 4, b, b, b, None, None, None) == m.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op():
+    L = m.lib()
+    s = _shape()
+    assert L.moe_route(ctypes.byref(s), 0, None, None, None, None, None, None, None, None, 0, None) == m.MOE_OK
+    assert L.moe_combine(ctypes.byref(s), 0, None, None, None, None, None, None) == m.MOE_OK
+    assert L.moe_expert_gate_up(ctypes.byref(s), 0, *([None] * 9), 0, None) == m.MOE_OK
+    assert L.moe_expert_down(ctypes.byref(s), 0, *([None] * 7), 0, None) == m.MOE_OK
+    assert L.moe_forward(ctypes.byref(s), 0, *([None] * 15), 0, None, 0, None) == m.MOE_OK
+    assert L.moe_workspace_size(ctypes.byref(s), 0) == 0 or L.moe_workspace_size(ctypes.byref(s), 0) < 4096
+
+
+def test_wait_limit_setter():
+    assert m.lib().moe_set_wait_limit_ns(0) == m.MOE_ERR_INVALID_ARG
+    assert m.lib().moe_set_wait_limit_ns(2_000_000_000) == m.MOE_OK
+
+
+def test_imbalance_ratio():
+    assert m.moe_eplb_imbalance([10, 10, 10, 10]) == 1.0
+    assert m.moe_eplb_imbalance([0, 0]) == 0.0
+    assert abs(m.moe_eplb_imbalance([30, 10, 10, 10]) - 2.0) < 1e-12
+
+
+def test_replica_plan_agrees_with_oracle():
+    rng = np.random.default_rng(1)
+    w = mi.WORKLOADS["redundant_t1024"]
+    for trial in range(200):
+        if trial % 3 == 0:
+            counts = rng.integers(0, 5, size=w.n_experts)      # many ties
+        elif trial % 3 == 1:
+            counts = (rng.pareto(1.2, size=w.n_experts) * 20).astype(np.int64)
+        else:
+            counts = np.zeros(w.n_experts, dtype=np.int64)
+            counts[rng.choice(32, 8, replace=False)] = rng.integers(1, 100, size=8)  # all hot in block 0
+        n_rep = int(rng.integers(0, 9))
+        got = m.moe_eplb_plan_replicas(w, counts, n_rep)
+        want = oracle.plan_replicas(w, counts, n_rep)
+        assert np.array_equal(got, want), (trial, counts, n_rep)
+    tiny = mi.WORKLOADS["tiny"].with_(n_blocks=4, n_slots=12)
+    got = m.moe_eplb_plan_replicas(tiny, np.array([10, 1, 7, 0, 3, 3, 9, 2]), 3)
+    assert list(got) == [5, -1, 8, -1, -1, -1, 2, -1]
+    with pytest.raises(m.MoeError):
+        m.moe_eplb_plan_replicas(tiny, np.zeros(8), 5)
