@@ -1,0 +1,453 @@
+"""Benchmark of the MoE layer forward pass on GB300 (one JSON line on rank 0).
+
+Default workload: the DeepSeek-V3 MoE layer decode step (T=32 tokens, hidden
+7168, 256 routed experts SwiGLU 2048, top-8, 2 shared experts, bf16,
+near-uniform routing), every input resident in HBM.  One step = one forward
+pass of the layer over the batch: router GEMM + top-k, dispatch, expert
+gate/up, expert down, combine (7 kernels of libmoe).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this
+project) on the host cores on a bounded sample of the same workload.
+With N > 1 (torchrun), every rank runs an independent replica of the layer
+on its own batch (weak scaling, no collective on the data path); the step
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and % of roofline (HBM GB/s decode, TFLOPS prefill), 1 GB300"
+DEFAULT_CONFIG = "decode_t32"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------------------ helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("grouped_gemm.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "moe_expert_layer_06_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        e = d[kernel][workload]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def layer_bytes_flops(w, counts_np):
+    """Algorithmic bytes and flops of one layer pass (touched expert weights read once)."""
+    H, I, E, k, T = w.hidden, w.inter, w.n_experts, w.top_k, w.tokens
+    touched = int((counts_np[:w.n_slots] > 0).sum())
+    expert_bytes = 3 * H * I * 2
+    shared_bytes = w.n_shared * 3 * H * w.inter_shared * 2
+    act = T * H * 2 + 2 * T * k * H * 2 + 2 * T * k * H * 2 + T * H * 2
+    B = touched * expert_bytes + shared_bytes + E * H * 2 + act
+    F = 6 * H * I * T * k + 6 * H * w.inter_shared * w.n_shared * T + 2 * T * H * E
+    # gate/up launch: gate+up weights of touched slots and shared, x_disp + x read, h written
+    B_gu = touched * 2 * H * I * 2 + w.n_shared * 2 * H * w.inter_shared * 2 + T * k * H * 2 + T * H * 2 + \
+        T * k * I * 2 + T * w.n_shared * w.inter_shared * 2
+    return dict(touched=touched, bytes=B, flops=F, gate_up_bytes=B_gu)
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import moe_expert_layer_06_gb300 as m
+    if rank == 0:
+        m.build_library()
+    if world > 1:
+        torch.distributed.barrier()
+    m.build_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = mi.WORKLOADS[args.config]
+    T = w.tokens
+    rep = None
+    if w.n_slots > w.n_experts:
+        rep = replica_plan_gpu(m, w, dev)
+    x = mi.hidden_states(w, device=dev)
+    wr = mi.router_weight(w, device=dev)
+    b = mi.router_bias(w)
+    bias = torch.from_numpy(b).to(dev) if b is not None else None
+    wg, wu, wd = mi.stacked_expert_weights(w, rep, device=dev)
+    sg, su, sd = mi.stacked_shared_weights(w, device=dev)
+    mi.clear_cache()
+    repd = torch.from_numpy(rep).to(dev) if rep is not None else None
+    torch.cuda.empty_cache()
+
+    k, H, I, S, E = w.top_k, w.hidden, w.inter, w.n_slots, w.n_experts
+    n = T * k
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx = torch.empty((T, k), **i32)
+    tw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    slot_of = torch.empty(n, **i32)
+    counts = torch.empty(S + 1, **i32)
+    blocks = torch.empty(w.n_blocks, **i32)
+    offsets = torch.empty(S + 2, **i32)
+    perm = torch.empty(n, **i32)
+    inv = torch.empty(n, **i32)
+    x_disp = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((n, I), dtype=torch.bfloat16, device=dev)
+    hs = torch.empty((T, w.n_shared * w.inter_shared), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+    ysh = torch.empty((T, H), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    rws = torch.empty(max(16, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        m.moe_route(w, T, x, wr, bias, None, None, idx, tw, rws)
+        m.moe_dispatch(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x_disp)
+        if ev is not None:
+            ev[0].record(stream)
+        m.moe_expert_gate_up(w, T, x, x_disp, offsets, wg, wu, sg, su, h, hs)
+        if ev is not None:
+            ev[1].record(stream)
+        m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh)
+        m.moe_combine(w, T, y, inv, tw, ysh, out)
+
+    launches_per_step = 7
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    rc = m.moe_check_status(stream)
+    if rc != 0:
+        raise RuntimeError("device status after warm-up: " + m.last_error())
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    elapsed_ms = t0.elapsed_time(t1)
+    gu_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    rc = m.moe_check_status(stream)
+    if rc != 0:
+        raise RuntimeError("device status after timing: " + m.last_error())
+
+    # end-to-end through the public C-ABI call with host buffers (pinned), copies inside the timed region
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_e2e = torch.empty_like(x)
+    ws = torch.empty(m.moe_workspace_size(w, T), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        x_e2e.copy_(x_host, non_blocking=True)
+        m.moe_forward(w, T, x_e2e, wr, bias, repd, wg, wu, wd, sg, su, sd, out, ws=ws)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    if m.moe_check_status(stream) != 0:
+        raise RuntimeError("device status after e2e: " + m.last_error())
+
+    if rank != 0:
+        return None
+    cnt = counts.cpu().numpy()
+    bf = layer_bytes_flops(w, cnt)
+    hbm, tf_burst, tf_sus, src = peaks()
+    ms_step = elapsed_ms / args.steps
+    t_roof_ms = max(bf["bytes"] / (hbm * 1e9), bf["flops"] / (tf_sus * 1e12)) * 1e3
+    achieved = bf["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
+    tokens = T * world
+    res = {
+        "metric": METRIC,
+        "value": round(tokens / (ms_step * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init DeepSeek-V3 MoE layer weights)",
+        "config": {
+            "workload": w.name, "description": w.description, "tokens": T, "hidden": H, "inter": I,
+            "n_experts": E, "top_k": k, "n_shared": w.n_shared, "n_slots": S,
+            "touched_slots": bf["touched"],
+            "l2": "inputs larger than L2: each step streams %.1f GB of touched expert weights" % (bf["bytes"] / 1e9),
+            "parallelism": "replica x%d (independent layer per GPU)" % world,
+        },
+        "us_per_layer": round(ms_step * 1e3, 2),
+        "layer_roofline": {
+            "bound": "hbm" if bf["bytes"] / (hbm * 1e9) >= bf["flops"] / (tf_sus * 1e12) else "tensor",
+            "algorithmic_bytes": bf["bytes"], "flops": bf["flops"], "t_roof_us": round(t_roof_ms * 1e3, 2),
+            "frac": round(t_roof_ms / ms_step, 4), "peaks": src,
+        },
+        "roofline": {
+            "kernel": "grouped_gemm_kernel<gate_up> (moe_expert_gate_up)",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm, 4),
+            "traffic": recorded_traffic("gate_up", w.name),
+            "algorithmic_bytes_per_launch": bf["gate_up_bytes"],
+            "avg_launch_us": round(gu_ms * 1e3, 2),
+            "peak_source": src + " (hbm_gbs, copy bandwidth)",
+        },
+        "e2e": {
+            "value": round(tokens / (e2e_ms / args.steps * 1e-3), 1),
+            "unit": "tokens/s",
+            "h2d_bytes_per_step": T * H * 2,
+            "d2h_bytes_per_step": T * H * 2,
+            "api": "moe_forward (C ABI) with pinned host input/output copies in the timed region",
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, dev, args.cpu_sample)
+    return res
+
+
+def replica_plan_gpu(m, w, dev):
+    """Replica map from the histogram of the skewed decode batch, through libmoe."""
+    src = mi.WORKLOADS[mi.REPLICA_PLAN_SOURCE]
+    x = mi.hidden_states(src, device=dev)
+    wr = mi.router_weight(src, device=dev)
+    b = torch.from_numpy(mi.router_bias(src)).to(dev)
+    idx = torch.empty((src.tokens, src.top_k), dtype=torch.int32, device=dev)
+    tw = torch.empty((src.tokens, src.top_k), dtype=torch.float32, device=dev)
+    ws = torch.empty(m.moe_route_workspace_size(src, src.tokens), dtype=torch.uint8, device=dev)
+    m.moe_route(src, src.tokens, x, wr, b, None, None, idx, tw, ws)
+    counts = torch.empty(src.n_slots + 1, dtype=torch.int32, device=dev)
+    m.moe_expert_histogram(src, src.tokens, idx, None, counts, None)
+    c = counts.cpu().numpy()[:src.n_experts]
+    return m.moe_eplb_plan_replicas(w, c, w.n_slots - w.n_experts)
+
+
+# ------------------------------------------------------------------------------ CPU oracle (baseline)
+
+def _oracle_sample_inputs(w, n_tok, dev):
+    """Inputs for the oracle on the first n_tok tokens (weights of the experts they use)."""
+    import oracle
+    toks = list(range(min(n_tok, w.tokens)))
+    x = mi.hidden_states(w, rows=slice(0, len(toks)))
+    wr = mi.router_weight(w)
+    b = mi.router_bias(w)
+    lo = oracle.router_logits(w, x, wr, b)
+    idx, _ = oracle.topk_softmax(lo, w.top_k)
+    gen_dev = dev if dev is not None else "cpu"
+    experts = {}
+    for e in sorted(set(int(v) for v in idx.ravel())):
+        experts[e] = tuple(t.cpu() for t in mi.expert_weights(w, e, device=gen_dev))
+    sh = tuple(t.cpu() for t in mi.stacked_shared_weights(w, device=gen_dev))
+    mi.clear_cache()
+    return toks, x, wr, b, experts, sh
+
+
+def _oracle_tokens(w, toks, x, wr, b, experts, sh, threads):
+    """The oracle's layer output for the sampled tokens: router, top-k, experts, shared, combine."""
+    import oracle
+
+    def one(i):
+        lo = oracle.router_logits(w, x[i:i + 1], wr, b)
+        idx, wt = oracle.topk_softmax(lo, w.top_k)
+        gud = [experts[int(e)] for e in idx[0]]
+        return oracle.token_output(w, x[i], wt[0], gud, *sh)
+
+    with cf.ThreadPoolExecutor(threads) as ex:
+        return list(ex.map(one, range(len(toks))))
+
+
+def cpu_baseline(w, dev, n_tok):
+    threads = max(1, min(os.cpu_count() or 1, n_tok))
+    toks, x, wr, b, experts, sh = _oracle_sample_inputs(w, n_tok, dev)
+    t = time.perf_counter()
+    _oracle_tokens(w, toks, x, wr, b, experts, sh, threads)
+    dt = time.perf_counter() - t
+    return {"value": round(len(toks) / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"full layer output (router, top-{w.top_k}, {w.top_k} expert FFNs, shared, combine) of the "
+                      f"first {len(toks)} tokens of the {w.name} batch, fp64 C oracle, one token per thread",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = mi.WORKLOADS[args.config]
+    n_tok = args.cpu_sample
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    threads = max(1, min(os.cpu_count() or 1, n_tok))
+    toks, x, wr, b, experts, sh = _oracle_sample_inputs(w, n_tok, dev)
+    for _ in range(args.warmup):
+        _oracle_tokens(w, toks, x, wr, b, experts, sh, threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_tokens(w, toks, x, wr, b, experts, sh, threads)
+    dt = (time.perf_counter() - t) / max(1, args.steps)
+    v = round(len(toks) / dt, 3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": w.name, "description": w.description, "tokens_per_step": len(toks)},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {len(toks)} tokens of the {w.name} batch per step, fp64 C oracle, "
+                                   f"one token per thread"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(mi.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        res = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

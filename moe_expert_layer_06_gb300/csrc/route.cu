@@ -1,5 +1,5 @@
 // Router tail: sum of the router GEMM's K-split partial logits (fixed order),
-// bias, softmax over all experts and top-k selection, one warp per token.
+// bias, softmax over all experts and top-k selection, one CTA per token.
 //
 // Blog post "专家并行(EP)", section 2.2: step 1 picks the top-8 of the 256
 // router logits; step 5 weights each selected expert's output by
@@ -16,89 +16,100 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
-template <int EPL>  // logits per lane; expert e = i*32 + lane
+// One CTA per token (grid-stride): all threads sum the K-split partials of one
+// expert each (coalesced over experts) into shared memory, then warp 0 runs
+// the softmax and the k arg-max rounds.
+template <int EPL>  // logits per lane of warp 0; expert e = i*32 + lane
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ partials, int ksplit,
                                                    const float* __restrict__ bias, int T, int E, int k,
                                                    float* __restrict__ logits_out,
                                                    int32_t* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w) {
+    __shared__ float lg[EPL * 32];
     const int lane = threadIdx.x & 31;
-    const int warps_per_block = blockDim.x >> 5;
     const size_t slice = (size_t)T * E;
-    for (int t = blockIdx.x * warps_per_block + (threadIdx.x >> 5); t < T; t += gridDim.x * warps_per_block) {
-        float v[EPL];
-        uint32_t valid = 0;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = i * 32 + lane;
-            float s = 0.0f;
-            if (e < E) {
-                const float* p = partials + (size_t)t * E + e;
-                s = p[0];
-                for (int ks = 1; ks < ksplit; ++ks) s += p[ks * slice];
-                if (bias) s += bias[e];
-                valid |= 1u << i;
-                if (logits_out) logits_out[(size_t)t * E + e] = s;
-            }
-            v[i] = s;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const float* p = partials + (size_t)t * E + e;
+            float s = p[0];
+            for (int ks = 1; ks < ksplit; ++ks) s += p[ks * slice];
+            if (bias) s += bias[e];
+            lg[e] = s;
+            if (logits_out) logits_out[(size_t)t * E + e] = s;
         }
-        // softmax statistics over all E (fixed reduction order)
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (valid & (1u << i)) mx = fmaxf(mx, v[i]);
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-        float den = 0.0f;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (valid & (1u << i)) den += expf(v[i] - mx);
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(0xffffffffu, den, d);
-        const float inv_den = 1.0f / den;
-
-        uint32_t avail = valid;
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            float v[EPL];
+            uint32_t valid = 0;
 #pragma unroll
             for (int i = 0; i < EPL; ++i) {
-                if (avail & (1u << i)) {
-                    const int e = i * 32 + lane;
-                    if (bi == 0x7fffffff || better(v[i], e, bv, bi)) {
-                        bv = v[i];
-                        bi = e;
+                const int e = i * 32 + lane;
+                v[i] = 0.0f;
+                if (e < E) {
+                    v[i] = lg[e];
+                    valid |= 1u << i;
+                }
+            }
+            // softmax statistics over all E (fixed reduction order)
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (valid & (1u << i)) mx = fmaxf(mx, v[i]);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+            float den = 0.0f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (valid & (1u << i)) den += expf(v[i] - mx);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(0xffffffffu, den, d);
+            const float inv_den = 1.0f / den;
+
+            uint32_t avail = valid;
+            for (int j = 0; j < k; ++j) {
+                float bv = -INFINITY;
+                int bi = 0x7fffffff;
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    if (avail & (1u << i)) {
+                        const int e = i * 32 + lane;
+                        if (bi == 0x7fffffff || better(v[i], e, bv, bi)) {
+                            bv = v[i];
+                            bi = e;
+                        }
                     }
                 }
-            }
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-                if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
-                    bv = ov;
-                    bi = oi;
+                for (int d = 16; d > 0; d >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+                    if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
+                        bv = ov;
+                        bi = oi;
+                    }
+                }
+                if (bi != 0x7fffffff && (bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+                if (lane == 0) {
+                    topk_idx[(size_t)t * k + j] = bi;
+                    topk_w[(size_t)t * k + j] = expf(bv - mx) * inv_den;
                 }
             }
-            if (bi != 0x7fffffff && (bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-            if (lane == 0) {
-                topk_idx[(size_t)t * k + j] = bi;
-                topk_w[(size_t)t * k + j] = expf(bv - mx) * inv_den;
-            }
         }
+        __syncthreads();
     }
 }
 
 template <int EPL>
 cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int T, int E, int k,
                        float* logits_out, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
-    const int warps = 8;
-    int blocks = (T + warps - 1) / warps;
+    int threads = ((E + 31) / 32) * 32;
+    if (threads > 256) threads = 256;
+    int blocks = T;
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    topk_kernel<EPL><<<blocks, warps * 32, 0, stream>>>(partials, ksplit, bias, T, E, k, logits_out, topk_idx,
-                                                        topk_w);
+    topk_kernel<EPL><<<blocks, threads, 0, stream>>>(partials, ksplit, bias, T, E, k, logits_out, topk_idx,
+                                                     topk_w);
     return cudaGetLastError();
 }
 

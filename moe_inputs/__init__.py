@@ -119,6 +119,24 @@ def normal_bf16(shape, std: float, seed: int, tensor_id: int, expert: int = 0,
     return (z * scale).to(torch.bfloat16).reshape(shape)
 
 
+def normal_bf16_experts(shape, std: float, seed: int, tensor_id: int, experts, device="cpu") -> torch.Tensor:
+    """normal_bf16 for several streams at once: result [len(experts), *shape].
+
+    Row e of the result equals normal_bf16(shape, std, seed, tensor_id, experts[e]).
+    """
+    n = int(np.prod(shape))
+    device = torch.device(device)
+    keys = torch.tensor([stream_key(seed, tensor_id, int(e)) for e in experts], dtype=torch.int64, device=device)
+    base = _hashed_counter(n, device)
+    o = _pcg(base[None, :] ^ keys[:, None])
+    s = (o & 255) + ((o >> 8) & 255) + ((o >> 16) & 255) + (o >> 24)
+    del o
+    z = (s - _IH_MEAN).to(torch.float32)
+    del s
+    scale = torch.tensor(float(np.float32(std / _IH_STD)), dtype=torch.float32, device=device)
+    return (z * scale).to(torch.bfloat16).reshape((len(experts),) + tuple(shape))
+
+
 def uniform_f32(shape, lo: float, hi: float, seed: int, tensor_id: int, expert: int = 0,
                 device="cpu") -> torch.Tensor:
     """Float32 values on a 2**-24 grid of [lo, hi) from the same hash stream."""
@@ -268,13 +286,16 @@ def stacked_expert_weights(w: Workload, replica_of: Optional[np.ndarray] = None,
     wu = torch.zeros((S, I, H), dtype=torch.bfloat16, device=device)
     wd = torch.zeros((S, H, I), dtype=torch.bfloat16, device=device)
     se = slot_experts(w, replica_of)
-    for s in range(S):
-        if se[s] < 0 or (slots is not None and s not in slots):
-            continue
-        g, u, d = expert_weights(w, int(se[s]), device)
-        wg[s].copy_(g)
-        wu[s].copy_(u)
-        wd[s].copy_(d)
+    todo = [s for s in range(S) if se[s] >= 0 and (slots is None or s in slots)]
+    # several experts per generator call on a GPU (fewer launches), one at a time on the host
+    batch = max(1, min(16, (1 << 27) // max(1, H * I))) if device.type == "cuda" else 1
+    for i in range(0, len(todo), batch):
+        sl = todo[i:i + batch]
+        ex = [int(se[s]) for s in sl]
+        idx = torch.tensor(sl, dtype=torch.int64, device=device)
+        wg.index_copy_(0, idx, normal_bf16_experts((I, H), 1.0 / math.sqrt(H), w.seed, TID_GATE, ex, device))
+        wu.index_copy_(0, idx, normal_bf16_experts((I, H), 1.0 / math.sqrt(H), w.seed, TID_UP, ex, device))
+        wd.index_copy_(0, idx, normal_bf16_experts((H, I), 1.0 / math.sqrt(I), w.seed, TID_DOWN, ex, device))
     return wg, wu, wd
 
 

@@ -48,6 +48,31 @@ def topk_gap(logits: np.ndarray, k: int) -> np.ndarray:
     return s[:, k - 1] - s[:, k]
 
 
+def check_topk(idx_gpu, idx_ref, logits_ref, k, gap=TOPK_GAP):
+    """Top-k parity where rounding cannot decide it.
+
+    The selected set must match on every token whose k-th and (k+1)-th oracle
+    logits differ by more than ``gap``; the order must match too where every
+    adjacent pair among the top k+1 differs by more than ``gap``.  Returns the
+    boolean mask of tokens whose set was checked.
+    """
+    idx_gpu = np.asarray(idx_gpu)
+    idx_ref = np.asarray(idx_ref)
+    s = -np.sort(-np.asarray(logits_ref), axis=1)[:, :k + 1]
+    adj = s[:, :-1] - s[:, 1:]
+    if s.shape[1] > k:
+        set_ok = adj[:, k - 1] > gap
+        order_ok = adj.min(axis=1) > gap
+    else:
+        set_ok = np.ones(s.shape[0], bool)
+        order_ok = adj.min(axis=1) > gap if adj.shape[1] else set_ok
+    bad_set = np.flatnonzero(set_ok & np.any(np.sort(idx_gpu, 1) != np.sort(idx_ref, 1), axis=1))
+    assert bad_set.size == 0, f"top-k set differs on {bad_set.size} tokens with gap > {gap}: {bad_set[:8]}"
+    bad_ord = np.flatnonzero(order_ok & np.any(idx_gpu != idx_ref, axis=1))
+    assert bad_ord.size == 0, f"top-k order differs on {bad_ord.size} tokens with all gaps > {gap}: {bad_ord[:8]}"
+    return set_ok
+
+
 def parallel_router_logits(w, x_cpu, wr_cpu, bias):
     """Oracle logits for all rows, rows split across host threads (the C code is pure)."""
     T = x_cpu.shape[0]
