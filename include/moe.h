@@ -201,6 +201,31 @@ MOE_API int moe_expert_ffn(const moe_shape_t* shape, int T, const void* x, const
                    const void* ws_up, const void* ws_down, void* y_disp, float* y_shared, int mode, void* ws,
                    size_t ws_bytes, void* stream);
 
+/* Capacity of the fixed device scratch used by moe_expert_ffn_noalloc (bytes). */
+#define MOE_FFN_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* moe_expert_ffn without a workspace, for callers that cannot allocate device
+ * memory (for instance a plugin whose host program owns every allocation and
+ * passes it only inputs and outputs, or a latency-critical path where
+ * cudaMalloc's implicit device synchronisation is not acceptable).  The
+ * expert-parallel post has no counterpart to this entry point.
+ * Same arguments, layouts and results as moe_expert_ffn, minus ws/ws_bytes:
+ * the SwiGLU intermediate (T*k*I*2 bytes rounded up to 256, plus
+ * T*n_sh*I_sh*2) lives in a fixed array of MOE_FFN_NOALLOC_SCRATCH_BYTES in
+ * the library's device memory, which every GPU that loads the library holds
+ * until the process exits.  Larger T returns MOE_ERR_UNSUPPORTED (8 MiB holds
+ * T <= 204 at the DeepSeek-V3 shape, k=8, I=2048, two shared experts of 2048).
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  All calls share the array and each leaves its contents there:
+ * calls whose work may overlap on the GPU (other streams, other threads on the
+ * same device) race on it and must be serialised by the caller.  Allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library call). */
+MOE_API int moe_expert_ffn_noalloc(const moe_shape_t* shape, int T, const void* x, const void* x_disp,
+                                   const int32_t* offsets, const void* w_gate, const void* w_up,
+                                   const void* w_down, const void* ws_gate, const void* ws_up,
+                                   const void* ws_down, void* y_disp, float* y_shared, int mode, void* stream);
+
 /* ---------------------------------------------------------------- steps 4-5: combine
  * Section 2.2 steps 4-5 (shared expert gate taken as 1):
  *   out[t,:] = bf16( sum_{j<k} topk_w[t,j] * y_disp[inv_perm[t*k+j], :] + y_shared[t,:] ),

@@ -35,8 +35,11 @@ EXPORTS = (
     "moe_debug_expire_wait", "moe_route_workspace_size", "moe_route", "moe_expert_histogram",
     "moe_eplb_imbalance", "moe_eplb_plan_replicas", "moe_dispatch", "moe_expert_gate_up",
     "moe_expert_down", "moe_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
-    "moe_workspace_size", "moe_forward",
+    "moe_workspace_size", "moe_forward", "moe_expert_ffn_noalloc",
 )
+
+# capacity of the fixed scratch of moe_expert_ffn_noalloc (include/moe.h)
+MOE_FFN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class MoeError(RuntimeError):
@@ -76,6 +79,7 @@ _SIG = {
     "moe_expert_down": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_ffn_workspace_size": (_Z, [_P, _I]),
     "moe_expert_ffn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
+    "moe_expert_ffn_noalloc": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
     "moe_workspace_size": (_Z, [_P, _I]),
     "moe_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
@@ -211,6 +215,14 @@ def moe_expert_ffn(shape, T, x, x_disp, offsets, w_gate, w_up, w_down, ws_gate, 
     _check(lib().moe_expert_ffn(_shape(shape), T, _ptr(x), _ptr(x_disp), _ptr(offsets), _ptr(w_gate),
                                 _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
                                 _ptr(y_disp), _ptr(y_shared), mode, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_expert_ffn_noalloc(shape, T, x, x_disp, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, y_disp,
+                           y_shared, mode=MOE_FFN_AUTO, stream=None):
+    """moe_expert_ffn for callers that cannot allocate: the intermediate lives in libmoe's fixed scratch."""
+    _check(lib().moe_expert_ffn_noalloc(_shape(shape), T, _ptr(x), _ptr(x_disp), _ptr(offsets), _ptr(w_gate),
+                                        _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
+                                        _ptr(y_disp), _ptr(y_shared), mode, _stream(stream)))
 
 
 def moe_combine(shape, T, y_disp, inv_perm, topk_w, y_shared, out, stream=None):

@@ -7,6 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
 #include "common.cuh"
 
 namespace moe {
@@ -84,5 +85,10 @@ cudaError_t launch_combine(const uint16_t* y_disp, const int32_t* inv_perm, cons
                            cudaStream_t stream);
 
 int num_sms();
+
+// Error reporting and shape validation of the C ABI, for entry points defined
+// outside moe_api.cu.
+int api_fail(int code, const char* fmt, ...);
+int api_check_shape(const moe_shape_t* shape, int T);
 
 }  // namespace moe

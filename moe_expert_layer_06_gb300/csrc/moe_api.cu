@@ -448,6 +448,16 @@ __global__ void expire_wait_kernel(DevStatus st) {
     }
 }
 
+int api_fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int api_check_shape(const moe_shape_t* shape, int T) { return check_shape(shape, T); }
+
 }  // namespace moe
 
 using namespace moe;
