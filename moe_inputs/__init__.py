@@ -197,6 +197,17 @@ WORKLOADS = {
                            description="prefill T=4096 (one 4k-token prompt), uniform routing"),
     "redundant_t1024": _dsv3("redundant_t1024", 1024, 1.5, n_slots=264,
                              description="T=1024 skewed routing, 256+8 slots, 8 hottest experts replicated"),
+    # profiling cases: the same per-expert shapes and rows per expert with 32 experts
+    # (2.8 GB of expert weights), small enough for multi-pass hardware-counter captures
+    "decode_t32_e32": Workload(name="decode_t32_e32", tokens=32, hidden=7168, inter=2048, n_experts=32,
+                               top_k=8, n_shared=2, inter_shared=2048, n_slots=32, n_blocks=8,
+                               router_std=0.02, skew_alpha=0.0,
+                               description="profiling case: DeepSeek-V3 expert shapes, 32 experts, T=32"),
+    "prefill_t512_e32": Workload(name="prefill_t512_e32", tokens=512, hidden=7168, inter=2048, n_experts=32,
+                                 top_k=8, n_shared=2, inter_shared=2048, n_slots=32, n_blocks=8,
+                                 router_std=0.02, skew_alpha=0.0,
+                                 description="profiling case: DeepSeek-V3 expert shapes, 32 experts, "
+                                             "T=512 (128 rows per expert, as prefill T=4096)"),
 }
 
 # the skewed decode workload whose histogram chooses the 8 replicated experts
