@@ -21,46 +21,73 @@ __device__ __forceinline__ int home_slot(int e, int E, int S, int n_blocks) {
     return (e / epb) * spb + (e % epb);
 }
 
-// One CTA: index work for all T*k assignments (a = t*k + j).
+// Slot of assignment x = t*k + j: the replica for odd tokens of a replicated
+// expert, else the expert's home slot; S (the invalid bucket) for a bad id.
+__device__ __forceinline__ int slot_of_assignment(const DispatchArgs& a, int x, bool& bad) {
+    const int t = x / a.k;
+    const int e = a.topk_idx[x];
+    if (e < 0 || e >= a.E) {
+        bad = true;
+        return a.S;
+    }
+    int slot = home_slot(e, a.E, a.S, a.n_blocks);
+    if (a.replica_of && (t & 1)) {
+        const int r = a.replica_of[e];
+        if (r >= 0) {
+            if (r < a.S) slot = r;
+            else { slot = a.S; bad = true; }
+        }
+    }
+    return slot;
+}
+
+// One CTA: index work for all T*k assignments (a = t*k + j).  Warp w owns the
+// contiguous range [w*per, (w+1)*per) of assignments, so warp order is
+// assignment order.  Pass 1 counts per warp and slot; a scan over warps gives
+// each warp its first rank in every slot; pass 2 walks the range again in
+// order and hands out ranks (match_any groups equal slots within a step).
 __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const DispatchArgs a) {
     extern __shared__ int sm[];
-    const int NS = a.S + 1;  // slots + invalid bucket
-    int* cnt = sm;           // [NS]
-    int* base = cnt + NS;    // [NS + 1]
-    int* run = base + NS + 1;  // [NS]
-    int* wcnt = run + NS;    // [32][NS]
+    const int NS = a.S + 1;    // slots + invalid bucket
+    int* cnt = sm;             // [NS]
+    int* base = cnt + NS;      // [NS + 1]
+    int* wc = base + NS + 1;   // [32][NS]: per-warp counts, then per-warp next rank
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = a.T * a.k;
+    const int per = (n + 31) / 32;
+    const int r0 = min(n, warp * per), r1 = min(n, r0 + per);
+    int* mine = wc + warp * NS;
+    const unsigned lt_mask = (1u << lane) - 1u;
 
-    for (int i = tid; i < NS; i += kIdxThreads) {
-        cnt[i] = 0;
-        run[i] = 0;
-    }
+    for (int i = tid; i < 32 * NS; i += kIdxThreads) wc[i] = 0;
     __syncthreads();
 
-    // replica remap + histogram (shared-memory atomics: the counts do not depend on order)
     bool bad = false;
-    for (int x = tid; x < n; x += kIdxThreads) {
-        const int t = x / a.k;
-        const int e = a.topk_idx[x];
-        int slot;
-        if (e < 0 || e >= a.E) {
-            slot = a.S;
-            bad = true;
-        } else {
-            slot = home_slot(e, a.E, a.S, a.n_blocks);
-            if (a.replica_of && (t & 1)) {
-                const int r = a.replica_of[e];
-                if (r >= 0) {
-                    if (r < a.S) slot = r;
-                    else { slot = a.S; bad = true; }
-                }
-            }
+    for (int x0 = r0; x0 < r1; x0 += 32) {
+        const int x = x0 + lane;
+        const bool valid = x < r1;
+        int slot = -1;
+        if (valid) {
+            slot = slot_of_assignment(a, x, bad);
+            if (a.slot_of) a.slot_of[x] = slot;
         }
-        if (a.slot_of) a.slot_of[x] = slot;
-        atomicAdd(&cnt[slot], 1);
+        const unsigned peers = __match_any_sync(0xffffffffu, slot);
+        if (valid && (__ffs(peers) - 1) == lane) mine[slot] += __popc(peers);
+        __syncwarp();
     }
     if (bad) raise_status(a.st, kStatusInvalidExpert);
+    __syncthreads();
+
+    // per slot: exclusive prefix over warps; totals are the counts
+    for (int s = tid; s < NS; s += kIdxThreads) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int c = wc[w * NS + s];
+            wc[w * NS + s] = run;
+            run += c;
+        }
+        cnt[s] = run;
+    }
     __syncthreads();
 
     for (int i = tid; i < NS; i += kIdxThreads) a.counts[i] = cnt[i];
@@ -76,8 +103,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
 
     // exclusive prefix of counts over slots and the invalid bucket
     if (warp == 0) {
-        const int per = (NS + 31) / 32;
-        const int s0 = min(NS, lane * per), s1 = min(NS, s0 + per);
+        const int ps = (NS + 31) / 32;
+        const int s0 = min(NS, lane * ps), s1 = min(NS, s0 + ps);
         int sum = 0;
         for (int s = s0; s < s1; ++s) sum += cnt[s];
         int incl = sum;
@@ -96,32 +123,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
     __syncthreads();
     for (int i = tid; i <= NS; i += kIdxThreads) a.offsets[i] = base[i];
 
-    // stable ranks: tiles of 1024 assignments in order; within a tile, rank =
-    // earlier same-slot lanes of the warp + same-slot counts of earlier warps
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int tile = 0; tile < n; tile += kIdxThreads) {
-        const int x = tile + tid;
-        const bool valid = x < n;
-        const int slot = valid ? a.slot_of[x] : -1;
-        for (int i = tid; i < 32 * NS; i += kIdxThreads) wcnt[i] = 0;
-        __syncthreads();
+    bool bad2 = false;
+    for (int x0 = r0; x0 < r1; x0 += 32) {
+        const int x = x0 + lane;
+        const bool valid = x < r1;
+        const int slot = valid ? slot_of_assignment(a, x, bad2) : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, slot);
-        const int lane_rank = __popc(peers & lt_mask);
-        const bool leader = (__ffs(peers) - 1) == lane;
-        const bool lane_last = (31 - __clz(peers)) == lane;
-        if (valid && leader) wcnt[warp * NS + slot] = __popc(peers);
-        __syncthreads();
-        int before = 0, after = 0, r0 = 0;
         if (valid) {
-            for (int w = 0; w < warp; ++w) before += wcnt[w * NS + slot];
-            for (int w = warp + 1; w < 32; ++w) after += wcnt[w * NS + slot];
-            r0 = run[slot];
-            const int row = base[slot] + r0 + before + lane_rank;
+            const int row = base[slot] + mine[slot] + __popc(peers & lt_mask);
             a.perm[row] = x;
             a.inv_perm[x] = row;
         }
-        __syncthreads();
-        if (valid && lane_last && after == 0) run[slot] = r0 + before + lane_rank + 1;
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) mine[slot] += __popc(peers);
+        __syncwarp();
     }
 }
 
@@ -135,6 +150,7 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint4* __restri
         const int t = perm[row] / k;
         const uint4* src = x + (size_t)t * vec_per_row;
         uint4* dst = x_disp + (size_t)row * vec_per_row;
+#pragma unroll 4
         for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
     }
 }

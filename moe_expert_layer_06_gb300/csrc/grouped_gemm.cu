@@ -41,9 +41,14 @@ struct Item {
     int ks;      // router K split
 };
 
+// Gate/up items carry the gate and the up tile of the same 128 rows; down items
+// carry two consecutive 128-row tiles of W_d (256 output rows); router items one
+// tile.  Two weight tiles per stage keep twice the weight bytes in flight per
+// token-chunk byte.
 template <int MODE>
 struct Traits {
-    static constexpr int NA = (MODE == kGateUp) ? 2 : 1;
+    static constexpr int NA = (MODE == kRouter) ? 1 : 2;
+    static constexpr int kRowsPerItem = (MODE == kDown) ? 256 : 128;
 };
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
@@ -61,17 +66,15 @@ struct Config {
     static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;
     static constexpr int kTmemCols = pow2_at_least(kNumAcc * kAccCols);
     static constexpr int kBarBytes = (2 * STAGES + 2 * kNumAcc + 1) * 8;
-    static constexpr int kTableBytes = (3 * kMaxSlots + 8) * 4;
+    static constexpr int kTableBytes = (kMaxSlots + 4) * 4;
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + 16 + kTableBytes;
     static_assert(kTmemCols <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
 };
 
-// Shared-memory tables describing the routed items of this launch.
+// Shared-memory table of the routed items of this launch.
 struct Table {
     int* pre;   // [S+1] exclusive prefix of routed items per slot
-    int* cnt;   // [S]   rows per slot
-    int* offs;  // [S]   first dispatch row per slot
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -94,9 +97,10 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Tabl
         it.kc1 = min(a.kc_routed, it.kc0 + a.kc_split);
         return it;
     }
+    constexpr int RPI = Traits<MODE>::kRowsPerItem;
     if (i < n_sh_items) {
         const int chunks = cdiv(a.T, BN);
-        const int mb = cdiv(a.m_shared, 128);
+        const int mb = cdiv(a.m_shared, RPI);
         it.shared = 1;
         int r = i;
         if (MODE == kGateUp) {
@@ -105,7 +109,7 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Tabl
         } else {
             it.z = 0;
         }
-        it.m0 = (r / chunks) * 128;
+        it.m0 = (r / chunks) * RPI;
         it.row0 = (r % chunks) * BN;
         it.nrows = min(BN, a.T - it.row0);
         it.kc0 = 0;
@@ -121,13 +125,15 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Tabl
     }
     const int s = lo;
     const int l = i - tb.pre[s];
-    const int chunks = cdiv(tb.cnt[s], BN);
+    const int off = __ldg(a.offsets + s);
+    const int cnt = __ldg(a.offsets + s + 1) - off;
+    const int chunks = cdiv(cnt, BN);
     const int c = l % chunks;
     it.shared = 0;
     it.z = s;
-    it.m0 = (l / chunks) * 128;
-    it.row0 = tb.offs[s] + c * BN;
-    it.nrows = min(BN, tb.cnt[s] - c * BN);
+    it.m0 = (l / chunks) * RPI;
+    it.row0 = off + c * BN;
+    it.nrows = min(BN, cnt - c * BN);
     it.kc0 = 0;
     it.kc1 = a.kc_routed;
     return it;
@@ -149,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     uint64_t* mma_done = tempty + C::kNumAcc;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* table = reinterpret_cast<int*>(tmem_slot + 4);
-    Table tb{table, table + kMaxSlots + 1, table + 2 * kMaxSlots + 1};
+    Table tb{reinterpret_cast<int*>(tmem_slot + 4)};
+    constexpr int RPI = Traits<MODE>::kRowsPerItem;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     int n_sh_items = 0;
     if (MODE != kRouter && a.n_shared > 0) {
         const int chunks = cdiv(a.T, BN);
-        const int mb = cdiv(a.m_shared, 128);
+        const int mb = cdiv(a.m_shared, RPI);
         n_sh_items = (MODE == kGateUp ? a.n_shared : 1) * mb * chunks;
     }
     int n_items;
@@ -171,15 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int S = a.n_slots;
             const int per = cdiv(S, 32);
             const int s0 = min(S, lane * per), s1 = min(S, s0 + per);
-            const int mb = cdiv(a.m_routed, 128);
+            const int mb = cdiv(a.m_routed, RPI);
             int sum = 0;
-            for (int s = s0; s < s1; ++s) {
-                const int o = a.offsets[s];
-                const int c = a.offsets[s + 1] - o;
-                tb.cnt[s] = c;
-                tb.offs[s] = o;
-                sum += cdiv(c, BN) * mb;
-            }
+            for (int s = s0; s < s1; ++s) sum += cdiv(a.offsets[s + 1] - a.offsets[s], BN) * mb;
             int incl = sum;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             int run = incl - sum;
             for (int s = s0; s < s1; ++s) {
                 tb.pre[s] = run;
-                run += cdiv(tb.cnt[s], BN) * mb;
+                run += cdiv(a.offsets[s + 1] - a.offsets[s], BN) * mb;
             }
             if (lane == 31) tb.pre[S] = incl;
         }
@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         bmid = za;
                     }
                     tma_load_3d(smem_u32(sa), ma0, fb, ka, it.m0, za, pol_w);
-                    if (NA == 2) tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
+                    if (MODE == kGateUp) tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
+                    if (MODE == kDown) tma_load_3d(smem_u32(sa + kABytes), ma0, fb, ka, it.m0 + 128, za, pol_w);
                     for (int b = 0; b < nb; ++b)
                         tma_load_3d(smem_u32(sb + b * 2048), mb, fb, kb, bmid, it.row0 + 16 * b, pol_x);
                     if (++stage == STAGES) {
@@ -353,14 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int mrow = it.m0 + q * 32 + lane;
             const int mlim = it.shared ? a.m_shared : a.m_routed;
             const bool row_ok = mrow < mlim;
+            (void)row_ok;
             const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + acc * C::kAccCols;
             for (int g = half; g < nb; g += 2) {
-                float v0[16];
+                float v0[16], v1[16];
                 tmem_ld16(tl + g * 16, v0);
+                if (NA == 2) tmem_ld16(tl + BN + g * 16, v1);
+                tmem_ld_wait();
                 if (MODE == kGateUp) {
-                    float v1[16];
-                    tmem_ld16(tl + BN + g * 16, v1);
-                    tmem_ld_wait();
                     if (row_ok) {
                         __nv_bfloat16* dst;
                         int ld;
@@ -379,29 +380,32 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         }
                     }
                 } else {
-                    tmem_ld_wait();
-                    if (row_ok) {
+                    // NA consecutive 128-row output blocks (down: rows m0.. and m0+128..)
+#pragma unroll
+                    for (int hh = 0; hh < NA; ++hh) {
+                        const int row = mrow + hh * 128;
+                        if (row >= mlim) continue;
                         if (MODE == kRouter) {
-                            float* dst = reinterpret_cast<float*>(a.out) + (size_t)it.ks * a.T * a.out_ld + mrow;
+                            float* dst = reinterpret_cast<float*>(a.out) + (size_t)it.ks * a.T * a.out_ld + row;
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 const int col = g * 16 + j;
-                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_ld] = v0[j];
+                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_ld] = hh ? v1[j] : v0[j];
                             }
                         } else if (it.shared) {
-                            float* dst = reinterpret_cast<float*>(a.out_sh) + mrow;
+                            float* dst = reinterpret_cast<float*>(a.out_sh) + row;
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 const int col = g * 16 + j;
-                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_sh_ld] = v0[j];
+                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_sh_ld] = hh ? v1[j] : v0[j];
                             }
                         } else {
-                            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) + mrow;
+                            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) + row;
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 const int col = g * 16 + j;
                                 if (col < it.nrows)
-                                    dst[(size_t)(it.row0 + col) * a.out_ld] = __float2bfloat16_rn(v0[j]);
+                                    dst[(size_t)(it.row0 + col) * a.out_ld] = __float2bfloat16_rn(hh ? v1[j] : v0[j]);
                             }
                         }
                     }
@@ -453,14 +457,14 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, c
     if (bn == 32) {
         switch (mode) {
             case kGateUp: return launch_one<kGateUp, 32, 5>(args, grid, stream);
-            case kDown: return launch_one<kDown, 32, 8>(args, grid, stream);
+            case kDown: return launch_one<kDown, 32, 5>(args, grid, stream);
             case kRouter: return launch_one<kRouter, 32, 8>(args, grid, stream);
         }
-    } else if (bn == 256) {
+    } else if (bn == kPrefillBN) {
         switch (mode) {
-            case kGateUp: return launch_one<kGateUp, 256, 3>(args, grid, stream);
-            case kDown: return launch_one<kDown, 256, 4>(args, grid, stream);
-            case kRouter: return launch_one<kRouter, 256, 4>(args, grid, stream);
+            case kGateUp: return launch_one<kGateUp, kPrefillBN, 4>(args, grid, stream);
+            case kDown: return launch_one<kDown, kPrefillBN, 4>(args, grid, stream);
+            case kRouter: return launch_one<kRouter, kPrefillBN, 5>(args, grid, stream);
         }
     }
     return cudaErrorInvalidValue;

@@ -46,7 +46,12 @@ struct GemmArgs {
     DevStatus st;
 };
 
-// Launch the grouped GEMM for `mode` with token chunk bn (32 or 256).
+// Token chunk of the prefill variant: 160 rows covers every expert of a 4096-token
+// batch with uniform routing (128 +- 11 rows) in one chunk while leaving room
+// for 4 pipeline stages (128 KB of weights in flight per SM).
+constexpr int kPrefillBN = 160;
+
+// Launch the grouped GEMM for `mode` with token chunk bn (32 or kPrefillBN).
 cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, cudaStream_t stream);
 int gemm_max_slots();
 

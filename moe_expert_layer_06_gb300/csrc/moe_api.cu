@@ -162,8 +162,8 @@ static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStre
 
 static int ffn_bn(int T, int mode) {
     if (mode == MOE_FFN_DECODE) return 32;
-    if (mode == MOE_FFN_PREFILL) return 256;
-    return T <= 32 ? 32 : 256;
+    if (mode == MOE_FFN_PREFILL) return kPrefillBN;
+    return T <= 32 ? 32 : kPrefillBN;
 }
 
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -175,7 +175,7 @@ struct RoutePlan {
 
 static RoutePlan route_plan(const moe_shape_t* s, int T) {
     RoutePlan p;
-    p.bn = T <= 32 ? 32 : 256;
+    p.bn = T <= 32 ? 32 : kPrefillBN;
     const int kc = (s->hidden + 63) / 64;
     p.tiles = ((s->n_experts + 127) / 128) * ((T + p.bn - 1) / p.bn);
     const int want = std::max(1, (num_sms() + p.tiles - 1) / std::max(1, p.tiles));

@@ -1,5 +1,5 @@
 // Router tail: sum of the router GEMM's K-split partial logits (fixed order),
-// bias, softmax over all experts and top-k selection, one CTA per token.
+// bias, softmax over all experts and top-k selection, one warp per token.
 //
 // Blog post "专家并行(EP)", section 2.2: step 1 picks the top-8 of the 256
 // router logits; step 5 weights each selected expert's output by
@@ -16,29 +16,35 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
-// One CTA per token (grid-stride): all threads sum the K-split partials of one
-// expert each (coalesced over experts) into shared memory, then warp 0 runs
-// the softmax and the k arg-max rounds.
-template <int EPL>  // logits per lane of warp 0; expert e = i*32 + lane
+// Eight tokens per CTA (grid-stride): all threads sum the K-split partials of
+// the eight tokens' logits (coalesced over experts) into shared memory, then
+// warp w runs the softmax and the k arg-max rounds of token w.
+constexpr int kTokPerCta = 8;
+
+template <int EPL>  // logits per lane; expert e = i*32 + lane
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ partials, int ksplit,
                                                    const float* __restrict__ bias, int T, int E, int k,
                                                    float* __restrict__ logits_out,
                                                    int32_t* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w) {
-    __shared__ float lg[EPL * 32];
+    __shared__ float lg[kTokPerCta][EPL * 32];
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const size_t slice = (size_t)T * E;
-    for (int t = blockIdx.x; t < T; t += gridDim.x) {
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
-            const float* p = partials + (size_t)t * E + e;
+    for (int t0 = blockIdx.x * kTokPerCta; t0 < T; t0 += gridDim.x * kTokPerCta) {
+        const int nt = min(kTokPerCta, T - t0);
+        for (int q = threadIdx.x; q < nt * E; q += blockDim.x) {
+            const int tt = q / E, e = q - tt * E;
+            const float* p = partials + (size_t)(t0 + tt) * E + e;
             float s = p[0];
             for (int ks = 1; ks < ksplit; ++ks) s += p[ks * slice];
             if (bias) s += bias[e];
-            lg[e] = s;
-            if (logits_out) logits_out[(size_t)t * E + e] = s;
+            lg[tt][e] = s;
+            if (logits_out) logits_out[(size_t)(t0 + tt) * E + e] = s;
         }
         __syncthreads();
-        if (threadIdx.x < 32) {
+        if (warp < nt) {
+            const int t = t0 + warp;
             float v[EPL];
             uint32_t valid = 0;
 #pragma unroll
@@ -46,7 +52,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
                 const int e = i * 32 + lane;
                 v[i] = 0.0f;
                 if (e < E) {
-                    v[i] = lg[e];
+                    v[i] = lg[warp][e];
                     valid |= 1u << i;
                 }
             }
@@ -102,9 +108,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
 template <int EPL>
 cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int T, int E, int k,
                        float* logits_out, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
-    int threads = ((E + 31) / 32) * 32;
-    if (threads > 256) threads = 256;
-    int blocks = T;
+    const int threads = 256;
+    int blocks = (T + kTokPerCta - 1) / kTokPerCta;
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
