@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const CUtensorMap* ma0 = it.shared ? &a.sa0 : &a.a0;
                 const CUtensorMap* ma1 = it.shared ? &a.sa1 : &a.a1;
                 const CUtensorMap* mb = it.shared ? &a.sb : &a.b;
-                const int nb = (it.nrows + 15) >> 4;
-                const uint32_t bytes = NA * kABytes + nb * 2048;
+                // one box of BN token rows (rows past the chunk are loaded and ignored)
+                const uint32_t bytes = C::kStageBytes;
                 for (int kc = it.kc0; kc < it.kc1; ++kc) {
                     if (*abort_flag || !mbar_wait(smem_u32(&empty[stage]), phase ^ 1, limit)) {
                         ok = false;
@@ -266,8 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     tma_load_3d(smem_u32(sa), ma0, fb, ka, it.m0, za, pol_w);
                     if (MODE == kGateUp) tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
                     if (MODE == kDown) tma_load_3d(smem_u32(sa + kABytes), ma0, fb, ka, it.m0 + 128, za, pol_w);
-                    for (int b = 0; b < nb; ++b)
-                        tma_load_3d(smem_u32(sb + b * 2048), mb, fb, kb, bmid, it.row0 + 16 * b, pol_x);
+                    tma_load_3d(smem_u32(sb), mb, fb, kb, bmid, it.row0, pol_x);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
