@@ -16,28 +16,42 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
-// Eight tokens per CTA (grid-stride): all threads sum the K-split partials of
-// the eight tokens' logits (coalesced over experts) into shared memory, then
-// warp w runs the softmax and the k arg-max rounds of token w.
+// tpc (1..8) tokens per CTA, grid-stride: all threads sum the K-split partials
+// of the CTA's tokens (coalesced over experts, eight loads in flight, added in
+// split order) into shared memory, then warp w runs the softmax and the k
+// arg-max rounds of token w.  Few tokens (decode) use one token per CTA so
+// that enough CTAs share the partial sums.
 constexpr int kTokPerCta = 8;
+
+__device__ __forceinline__ float sum_partials(const float* p, int ksplit, size_t slice) {
+    float s = p[0];
+    int ks = 1;
+    for (; ks + 8 <= ksplit; ks += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(p + (size_t)(ks + u) * slice);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) s += v[u];
+    }
+    for (; ks < ksplit; ++ks) s += __ldg(p + (size_t)ks * slice);
+    return s;
+}
 
 template <int EPL>  // logits per lane; expert e = i*32 + lane
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ partials, int ksplit,
                                                    const float* __restrict__ bias, int T, int E, int k,
                                                    float* __restrict__ logits_out,
                                                    int32_t* __restrict__ topk_idx,
-                                                   float* __restrict__ topk_w) {
+                                                   float* __restrict__ topk_w, int tpc) {
     __shared__ float lg[kTokPerCta][EPL * 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const size_t slice = (size_t)T * E;
-    for (int t0 = blockIdx.x * kTokPerCta; t0 < T; t0 += gridDim.x * kTokPerCta) {
-        const int nt = min(kTokPerCta, T - t0);
+    for (int t0 = blockIdx.x * tpc; t0 < T; t0 += gridDim.x * tpc) {
+        const int nt = min(tpc, T - t0);
         for (int q = threadIdx.x; q < nt * E; q += blockDim.x) {
             const int tt = q / E, e = q - tt * E;
-            const float* p = partials + (size_t)(t0 + tt) * E + e;
-            float s = p[0];
-            for (int ks = 1; ks < ksplit; ++ks) s += p[ks * slice];
+            float s = sum_partials(partials + (size_t)(t0 + tt) * E + e, ksplit, slice);
             if (bias) s += bias[e];
             lg[tt][e] = s;
             if (logits_out) logits_out[(size_t)(t0 + tt) * E + e] = s;
@@ -109,12 +123,13 @@ template <int EPL>
 cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int T, int E, int k,
                        float* logits_out, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
     const int threads = 256;
-    int blocks = (T + kTokPerCta - 1) / kTokPerCta;
+    const int tpc = T <= 4 * num_sms() ? 1 : kTokPerCta;
+    int blocks = (T + tpc - 1) / tpc;
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     topk_kernel<EPL><<<blocks, threads, 0, stream>>>(partials, ksplit, bias, T, E, k, logits_out, topk_idx,
-                                                     topk_w);
+                                                     topk_w, tpc);
     return cudaGetLastError();
 }
 
