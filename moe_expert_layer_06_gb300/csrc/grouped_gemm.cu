@@ -18,7 +18,7 @@
 // round-robin; warp roles:
 //   warp 0      TMA producer (one elected lane)   smem ring of STAGES stages
 //   warp 1      MMA issuer   (one elected lane)   TMEM accumulators (x2 when they fit)
-//   warps 2..9  epilogue: tcgen05.ld -> SwiGLU / convert -> global stores
+//   warps 2..17 epilogue: tcgen05.ld -> SwiGLU / convert -> global stores
 // Every mbarrier wait is bounded; on expiry the kernel raises the status word,
 // drains its own copies and MMAs (bounded) and frees its TMEM.
 #include "kernels.h"
@@ -26,8 +26,8 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 320;        // 10 warps
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;          // 4 per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kABytes = 128 * 64 * 2;  // one 128x64 bf16 weight tile
 constexpr int kMaxSlots = 1024;
 
@@ -70,6 +70,7 @@ struct Config {
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + 16 + kTableBytes;
     static_assert(kTmemCols <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
+    static_assert(BN <= 15 * 16, "token chunk must be at most 15 groups of 16 rows");
 };
 
 // Shared-memory table of the routed items of this launch.
@@ -212,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&a.a0);
-        tma_prefetch_desc(&a.b);
+        tma_prefetch_desc(&a.b[0]);
         if (NA == 2) tma_prefetch_desc(&a.a1);
         if (MODE != kRouter && a.n_shared > 0) {
             tma_prefetch_desc(&a.sa0);
-            tma_prefetch_desc(&a.sb);
+            tma_prefetch_desc(&a.sb[0]);
             if (NA == 2) tma_prefetch_desc(&a.sa1);
         }
     }
@@ -243,9 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
                 const CUtensorMap* ma0 = it.shared ? &a.sa0 : &a.a0;
                 const CUtensorMap* ma1 = it.shared ? &a.sa1 : &a.a1;
-                const CUtensorMap* mb = it.shared ? &a.sb : &a.b;
-                // one box of BN token rows (rows past the chunk are loaded and ignored)
-                const uint32_t bytes = C::kStageBytes;
+                const CUtensorMap* mb = it.shared ? a.sb : a.b;
+                // the chunk's rows rounded up to 16, one box per set bit of the 16-row count
+                const int nb = (it.nrows + 15) >> 4;
+                const uint32_t bytes = NA * kABytes + nb * 2048;
                 for (int kc = it.kc0; kc < it.kc1; ++kc) {
                     if (*abort_flag || !mbar_wait(smem_u32(&empty[stage]), phase ^ 1, limit)) {
                         ok = false;
@@ -266,7 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     tma_load_3d(smem_u32(sa), ma0, fb, ka, it.m0, za, pol_w);
                     if (MODE == kGateUp) tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
                     if (MODE == kDown) tma_load_3d(smem_u32(sa + kABytes), ma0, fb, ka, it.m0 + 128, za, pol_w);
-                    tma_load_3d(smem_u32(sb), mb, fb, kb, bmid, it.row0, pol_x);
+                    for (int bit = 3, off = 0; bit >= 0; --bit) {
+                        if (nb & (1 << bit)) {
+                            tma_load_3d(smem_u32(sb + off * 2048), mb + bit, fb, kb, bmid, it.row0 + off * 16, pol_x);
+                            off += 1 << bit;
+                        }
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         // =========================== epilogue ================================
         const int ew = warp - 2;
         const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int half = ew >> 2;         // column groups: even (0) or odd (1)
+        const int part = ew >> 2;         // column groups part, part+4, ...
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const bool row_ok = mrow < mlim;
             (void)row_ok;
             const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + acc * C::kAccCols;
-            for (int g = half; g < nb; g += 2) {
+            for (int g = part; g < nb; g += kEpiWarps / 4) {
                 float v0[16], v1[16];
                 tmem_ld16(tl + g * 16, v0);
                 if (NA == 2) tmem_ld16(tl + BN + g * 16, v1);

@@ -19,14 +19,15 @@ enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2 };
 // tile of 128 output rows (the UMMA M operand), B is a chunk of up to BN
 // token rows (the UMMA N operand), K runs over 64-element chunks.  Every
 // operand is read by TMA through the tensor maps below (3-D, bf16, 128-byte
-// swizzle, box {64, rows, 1}).
+// swizzle; weights box {64, 128, 1}; tokens box {64, 1, 16 << j}, so a chunk of
+// n 16-row groups is loaded exactly with one box per set bit of n).
 struct GemmArgs {
     CUtensorMap a0;   // routed weights: gate [S,I,H] | down [S,H,I] | router [1,E,H]
     CUtensorMap a1;   // routed up weights [S,I,H] (gate/up only)
-    CUtensorMap b;    // routed activations: x_disp [T*k,H] | h_disp [T*k,I] | x [T,H]
+    CUtensorMap b[4]; // routed activations: x_disp [T*k,H] | h_disp [T*k,I] | x [T,H]; boxes of 16,32,64,128 rows
     CUtensorMap sa0;  // shared gate [n_sh,I_sh,H] | shared down [n_sh,H,I_sh]
     CUtensorMap sa1;  // shared up [n_sh,I_sh,H]
-    CUtensorMap sb;   // shared activations: x [T,H] | h_sh [T,n_sh,I_sh]
+    CUtensorMap sb[4];// shared activations: x [T,H] | h_sh [T,n_sh,I_sh]; same four box heights
     const int32_t* offsets;  // [S+2] dispatch row offsets (gate/up, down)
     int n_slots;
     int T;

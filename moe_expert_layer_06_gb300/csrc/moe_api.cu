@@ -112,16 +112,24 @@ static int tmap_weights(CUtensorMap* m, const void* p, int n, int rows, int K) {
                         64, 128, 1);
 }
 
-// activations [rows][K] -> dims {K, 1, rows}, box {64, 1, box_rows} (one token chunk)
-static int tmap_rows(CUtensorMap* m, const void* p, int rows, int K, int box_rows) {
-    return make_tmap_3d(m, p, (uint64_t)K, 1, (uint64_t)rows, (uint64_t)K * 2, (uint64_t)K * 2, 64, 1,
-                        (uint32_t)box_rows);
+// activations [rows][K] -> dims {K, 1, rows}; four maps with boxes {64, 1, 16 << j}
+static int tmap_rows(CUtensorMap* m, const void* p, int rows, int K) {
+    for (int j = 0; j < 4; ++j) {
+        const int rc = make_tmap_3d(m + j, p, (uint64_t)K, 1, (uint64_t)rows, (uint64_t)K * 2, (uint64_t)K * 2,
+                                    64, 1, 16u << j);
+        if (rc) return rc;
+    }
+    return MOE_OK;
 }
 
-// shared intermediate [T][n_sh][I_sh] -> dims {I_sh, n_sh, T}, box {64, 1, box_rows}
-static int tmap_hsh(CUtensorMap* m, const void* p, int T, int n_sh, int I_sh, int box_rows) {
-    return make_tmap_3d(m, p, (uint64_t)I_sh, (uint64_t)n_sh, (uint64_t)T, (uint64_t)I_sh * 2,
-                        (uint64_t)I_sh * n_sh * 2, 64, 1, (uint32_t)box_rows);
+// shared intermediate [T][n_sh][I_sh] -> dims {I_sh, n_sh, T}; boxes {64, 1, 16 << j}
+static int tmap_hsh(CUtensorMap* m, const void* p, int T, int n_sh, int I_sh) {
+    for (int j = 0; j < 4; ++j) {
+        const int rc = make_tmap_3d(m + j, p, (uint64_t)I_sh, (uint64_t)n_sh, (uint64_t)T, (uint64_t)I_sh * 2,
+                                    (uint64_t)I_sh * n_sh * 2, 64, 1, 16u << j);
+        if (rc) return rc;
+    }
+    return MOE_OK;
 }
 
 // ------------------------------------------------------------------ validation
@@ -221,10 +229,10 @@ static int route_impl(const moe_shape_t* s, int T, const void* x, const void* w_
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_router, 1, s->n_experts, s->hidden))) return rc;
-    if ((rc = tmap_rows(&g.b, x, T, s->hidden, p.bn))) return rc;
+    if ((rc = tmap_rows(g.b, x, T, s->hidden))) return rc;
     g.a1 = g.a0;
     g.sa0 = g.sa1 = g.a0;
-    g.sb = g.b;
+    for (int j = 0; j < 4; ++j) g.sb[j] = g.b[j];
     g.T = T;
     g.m_routed = s->n_experts;
     g.kc_routed = (s->hidden + 63) / 64;
@@ -293,15 +301,15 @@ static int gate_up_impl(const moe_shape_t* s, int T, const void* x, const void* 
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_gate, s->n_slots, s->inter, s->hidden))) return rc;
     if ((rc = tmap_weights(&g.a1, w_up, s->n_slots, s->inter, s->hidden))) return rc;
-    if ((rc = tmap_rows(&g.b, x_disp, n, s->hidden, bn))) return rc;
+    if ((rc = tmap_rows(g.b, x_disp, n, s->hidden))) return rc;
     if (n_sh > 0) {
         if ((rc = tmap_weights(&g.sa0, ws_gate, n_sh, s->inter_shared, s->hidden))) return rc;
         if ((rc = tmap_weights(&g.sa1, ws_up, n_sh, s->inter_shared, s->hidden))) return rc;
-        if ((rc = tmap_rows(&g.sb, x, T, s->hidden, bn))) return rc;
+        if ((rc = tmap_rows(g.sb, x, T, s->hidden))) return rc;
     } else {
         g.sa0 = g.a0;
         g.sa1 = g.a1;
-        g.sb = g.b;
+        for (int j = 0; j < 4; ++j) g.sb[j] = g.b[j];
     }
     g.offsets = offsets;
     g.n_slots = s->n_slots;
@@ -343,14 +351,14 @@ static int down_impl(const moe_shape_t* s, int T, const void* h_disp, const void
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_down, s->n_slots, s->hidden, s->inter))) return rc;
-    if ((rc = tmap_rows(&g.b, h_disp, n, s->inter, bn))) return rc;
+    if ((rc = tmap_rows(g.b, h_disp, n, s->inter))) return rc;
     g.a1 = g.a0;
     if (n_sh > 0) {
         if ((rc = tmap_weights(&g.sa0, ws_down, n_sh, s->hidden, s->inter_shared))) return rc;
-        if ((rc = tmap_hsh(&g.sb, h_shared, T, n_sh, s->inter_shared, bn))) return rc;
+        if ((rc = tmap_hsh(g.sb, h_shared, T, n_sh, s->inter_shared))) return rc;
     } else {
         g.sa0 = g.a0;
-        g.sb = g.b;
+        for (int j = 0; j < 4; ++j) g.sb[j] = g.b[j];
     }
     g.sa1 = g.sa0;
     g.offsets = offsets;
