@@ -21,7 +21,7 @@
 // cleared between calls.
 #include <mutex>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "kernels.h"
 
 namespace moe {

@@ -8,7 +8,7 @@
 #include <algorithm>
 #include <vector>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "kernels.h"
 
 namespace moe {
