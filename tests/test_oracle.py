@@ -318,6 +318,14 @@ def test_replica_plan_rule_on_hand_worked_counts():
     assert list(rep) == [5, -1, 8, -1, -1, -1, 2, -1]
 
 
+def test_replica_plan_hot_list_ties_go_to_lower_id():
+    _, w = _replica_tiny()
+    # experts 1 and 2 tie at 5: expert 1 is hot.  Loads x2 (hot halved): block0 = 3*2 + 5 = 11,
+    # block1 = 5*2 = 10, blocks 2 and 3 = 0 -> block 2 (lower of the tie) -> slot 2*3 + 2 = 8
+    rep = oracle.plan_replicas(w, np.array([3, 5, 5, 0, 0, 0, 0, 0], dtype=np.int32), 1)
+    assert list(rep) == [-1, 8, -1, -1, -1, -1, -1, -1]
+
+
 def test_replica_plan_falls_back_to_home_block():
     _, w = _replica_tiny()
     counts = np.array([5, 6, 7, 8, 1, 2, 3, 4], dtype=np.int32)
