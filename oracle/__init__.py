@@ -118,6 +118,16 @@ def topk_softmax(logits, k: int):
     return idx, wt
 
 
+def topk_grouped(logits, k: int, n_groups: int, topk_groups: int):
+    lg = _f64(logits)
+    T, E = lg.shape
+    assert E % n_groups == 0 and topk_groups * (E // n_groups) >= k
+    idx = np.empty((T, k), dtype=np.int32)
+    wt = np.empty((T, k), dtype=np.float64)
+    lib().oracle_topk_grouped(T, E, k, n_groups, topk_groups, _ptr(lg), _ptr(idx), _ptr(wt))
+    return idx, wt
+
+
 def home_slot(w, e: int) -> int:
     return lib().oracle_home_slot(ctypes.byref(shape_of(w)), e)
 

@@ -79,6 +79,55 @@ void oracle_topk_softmax(int T, int E, int k, const double* logits, int32_t* idx
     free(taken);
 }
 
+/* Summary section of the post: route by expert group first, then by expert.
+ * Readings are stated in the header. */
+void oracle_topk_grouped(int T, int E, int k, int n_groups, int topk_groups, const double* logits,
+                         int32_t* idx, double* weight) {
+    const int gs = E / n_groups;
+    char* taken = (char*)malloc((size_t)E);
+    char* group_kept = (char*)malloc((size_t)n_groups);
+    double* gscore = (double*)malloc((size_t)n_groups * sizeof(double));
+    for (int t = 0; t < T; ++t) {
+        const double* l = logits + (size_t)t * E;
+        for (int g = 0; g < n_groups; ++g) {
+            double best = l[g * gs];
+            for (int e = g * gs + 1; e < (g + 1) * gs; ++e)
+                if (l[e] > best) best = l[e];
+            gscore[g] = best;
+            group_kept[g] = 0;
+        }
+        for (int r = 0; r < topk_groups; ++r) {
+            int bg = -1;
+            for (int g = 0; g < n_groups; ++g) {
+                if (group_kept[g]) continue;
+                if (bg < 0 || ranks_before(gscore[g], g, gscore[bg], bg)) bg = g;
+            }
+            group_kept[bg] = 1;
+        }
+        for (int e = 0; e < E; ++e) taken[e] = !group_kept[e / gs];
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || ranks_before(l[e], e, l[best], best)) best = e;
+            }
+            taken[best] = 1;
+            idx[(size_t)t * k + j] = best;
+        }
+        double mx = l[0];
+        for (int e = 1; e < E; ++e)
+            if (l[e] > mx) mx = l[e];
+        double denom = 0.0;
+        for (int e = 0; e < E; ++e) denom += exp(l[e] - mx);
+        if (weight)
+            for (int j = 0; j < k; ++j)
+                weight[(size_t)t * k + j] = exp(l[idx[(size_t)t * k + j]] - mx) / denom;
+    }
+    free(taken);
+    free(group_kept);
+    free(gscore);
+}
+
 /* Section 2.1: "each GPU holds a contiguous 1/N of the experts" (GPU g: experts
  * 32g..32g+31).  Section 6.3: with 8 redundant experts each of the 8 GPUs holds
  * 33.  Reading: a block keeps its own experts first, in order, and its replica

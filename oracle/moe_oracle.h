@@ -55,6 +55,17 @@ void oracle_router_logits(const oracle_shape* s, int T, const uint16_t* x,
  * combine weight softmax(logits over all E)[idx], not renormalised. */
 void oracle_topk_softmax(int T, int E, int k, const double* logits, int32_t* idx, double* weight);
 
+/* Group-limited top-k (the summary section of the expert-parallelism post
+ * names routing to an expert group first and to experts within it second as a
+ * direction for larger expert counts).
+ * Reading: the E experts form n_groups contiguous groups (the EP blocks); a
+ * group's score is its largest logit; the topk_groups best groups are kept
+ * (score descending, ties -> lower group); the top-k experts are then chosen
+ * among the kept groups' experts only (same order and tie rule as
+ * oracle_topk_softmax), and the combine weight is still softmax over all E. */
+void oracle_topk_grouped(int T, int E, int k, int n_groups, int topk_groups, const double* logits,
+                         int32_t* idx, double* weight);
+
 /* Home slot of logical expert e (blocks keep their experts in order; with
  * replicas each block has trailing replica slots). */
 int32_t oracle_home_slot(const oracle_shape* s, int32_t e);

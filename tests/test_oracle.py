@@ -96,6 +96,42 @@ def test_topk_tie_rule_hand_cases():
     assert list(idx[0]) == [2, 5, 4, 6, 0, 3]
 
 
+def test_grouped_topk_reduces_to_plain_topk():
+    rng = np.random.default_rng(5)
+    logits = rng.integers(-30, 30, size=(25, 64)).astype(np.float64) / 8.0
+    idx0, wt0 = oracle.topk_softmax(logits, 6)
+    for n_groups, topk_groups in ((8, 8), (64, 6), (1, 1), (4, 4)):
+        idx, wt = oracle.topk_grouped(logits, 6, n_groups, topk_groups)
+        assert np.array_equal(idx, idx0), (n_groups, topk_groups)
+        np.testing.assert_allclose(wt, wt0, rtol=1e-15)
+
+
+def test_grouped_topk_keeps_the_best_groups():
+    rng = np.random.default_rng(6)
+    T, E, k, G, Gk = 40, 64, 6, 8, 3
+    gs = E // G
+    logits = rng.integers(-40, 40, size=(T, E)).astype(np.float64) / 4.0  # ties at every level
+    idx, wt = oracle.topk_grouped(logits, k, G, Gk)
+    p = torch.softmax(torch.from_numpy(logits), dim=-1).numpy()
+    for t in range(T):
+        gmax = logits[t].reshape(G, gs).max(axis=1)
+        kept = sorted(range(G), key=lambda g: (-gmax[g], g))[:Gk]
+        allowed = [e for e in range(E) if e // gs in kept]
+        expect = sorted(allowed, key=lambda e: (-logits[t, e], e))[:k]
+        assert list(idx[t]) == expect
+        np.testing.assert_allclose(wt[t], p[t, idx[t]], rtol=1e-14)
+        assert len({int(e) // gs for e in idx[t]}) <= Gk
+
+
+def test_grouped_topk_hand_case():
+    # groups of 2: (5, 0) (5, 4) (1, 1) (0, 6); group maxima 5, 5, 1, 6
+    lg = np.array([[5.0, 0.0, 5.0, 4.0, 1.0, 1.0, 0.0, 6.0]])
+    idx, _ = oracle.topk_grouped(lg, 3, 4, 2)  # keep groups 3 (6) and 0 (5, lower than 1)
+    assert list(idx[0]) == [7, 0, 1]
+    idx, _ = oracle.topk_grouped(lg, 3, 4, 3)  # groups 3, 0, 1
+    assert list(idx[0]) == [7, 0, 2]
+
+
 def test_softmax_weights_are_not_renormalised():
     logits = np.array([[2.0, 1.0, 0.0, -1.0]])
     _, wt = oracle.topk_softmax(logits, 2)

@@ -29,6 +29,10 @@ MUTANTS = [
      "weight[(size_t)t * k + j] = exp(l[idx[(size_t)t * k + j]] - mx) / denom;",
      "weight[(size_t)t * k + j] = exp(l[idx[(size_t)t * k + j]] - mx) / (denom * 0.0 + 1.0) / "
      "(exp(l[idx[(size_t)t * k]] - mx) + (k > 1 ? exp(l[idx[(size_t)t * k + 1]] - mx) : 0.0));"),
+    ("group score is the group's smallest logit", "if (l[e] > best) best = l[e];\n            gscore[g] = best;",
+     "if (l[e] < best) best = l[e];\n            gscore[g] = best;"),
+    ("group ties go to the higher group", "if (bg < 0 || ranks_before(gscore[g], g, gscore[bg], bg)) bg = g;",
+     "if (bg < 0 || ranks_before(gscore[g], -g, gscore[bg], -bg)) bg = g;"),
     ("home slot ignores the replica slots", "return (e / epb) * spb + (e % epb);", "return e;"),
     ("replica used by even tokens", "replica_of[e] >= 0 && (t % 2) == 1", "replica_of[e] >= 0 && (t % 2) == 0"),
     ("dispatch fills slots in reverse order", "for (int a = 0; a < n; ++a) {\n        const int32_t slot = slot_of[a];",
@@ -56,6 +60,9 @@ PINS = [
     pins.test_topk_matches_bruteforce_sort_and_softmax,
     pins.test_topk_tie_rule_hand_cases,
     pins.test_softmax_weights_are_not_renormalised,
+    pins.test_grouped_topk_reduces_to_plain_topk,
+    pins.test_grouped_topk_keeps_the_best_groups,
+    pins.test_grouped_topk_hand_case,
     pins.test_worked_example_block_mapping,
     pins.test_home_slots_of_redundant_layout,
     pins.test_slot_map_replica_parity_and_invalid_ids,
