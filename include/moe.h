@@ -123,6 +123,19 @@ MOE_API int moe_route(const moe_shape_t* shape, int T, const void* x, const void
               const float* logits_in, float* logits_out, int32_t* topk_idx, float* topk_w, void* ws,
               size_t ws_bytes, void* stream);
 
+/* Group-limited routing (the post's summary section names routing by expert
+ * group first and by expert second as a direction for larger expert counts).
+ * The E experts form n_groups contiguous groups of E/n_groups (with
+ * n_groups = B these are the EP blocks); a group scores its largest logit;
+ * the topk_groups best groups are kept (ties -> lower group); topk_idx is the
+ * top-k of the kept groups' experts (same order and tie rule as moe_route);
+ * topk_w is still softmax over all E logits.  1 <= n_groups <= 32,
+ * n_groups divides E, 1 <= topk_groups <= n_groups, k <= topk_groups*E/n_groups.
+ * Other arguments, workspace and outputs as moe_route. */
+MOE_API int moe_route_grouped(const moe_shape_t* shape, int T, int n_groups, int topk_groups, const void* x,
+                              const void* w_router, const float* bias, const float* logits_in, float* logits_out,
+                              int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- EPLB monitor
  * "专家并行(EP)" section 6.2 ("monitor": tokens arriving at each expert; a
  * rank's load = sum over its experts) for one batch, and section 6.3 (a token

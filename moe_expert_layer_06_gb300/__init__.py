@@ -35,7 +35,7 @@ EXPORTS = (
     "moe_debug_expire_wait", "moe_route_workspace_size", "moe_route", "moe_expert_histogram",
     "moe_eplb_imbalance", "moe_eplb_plan_replicas", "moe_dispatch", "moe_expert_gate_up",
     "moe_expert_down", "moe_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
-    "moe_workspace_size", "moe_forward", "moe_expert_ffn_noalloc",
+    "moe_workspace_size", "moe_forward", "moe_expert_ffn_noalloc", "moe_route_grouped",
 )
 
 # capacity of the fixed scratch of moe_expert_ffn_noalloc (include/moe.h)
@@ -71,6 +71,7 @@ _SIG = {
     "moe_debug_expire_wait": (_I, [_P]),
     "moe_route_workspace_size": (_Z, [_P, _I]),
     "moe_route": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_route_grouped": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_histogram": (_I, [_P, _I, _P, _P, _P, _P, _P]),
     "moe_eplb_imbalance": (ctypes.c_double, [_P, _I]),
     "moe_eplb_plan_replicas": (_I, [_P, _P, _I, _P]),
@@ -164,6 +165,14 @@ def moe_route(shape, T, x, w_router, bias, logits_in, logits_out, topk_idx, topk
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(lib().moe_route(_shape(shape), T, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(logits_in),
                            _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_route_grouped(shape, T, n_groups, topk_groups, x, w_router, bias, logits_in, logits_out, topk_idx,
+                      topk_w, ws, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(lib().moe_route_grouped(_shape(shape), T, n_groups, topk_groups, _ptr(x), _ptr(w_router), _ptr(bias),
+                                   _ptr(logits_in), _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(ws),
+                                   ws_bytes, _stream(stream)))
 
 
 def moe_expert_histogram(shape, T, topk_idx, replica_of, counts, block_counts, stream=None):

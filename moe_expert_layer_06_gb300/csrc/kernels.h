@@ -63,9 +63,12 @@ int make_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, u
                  uint32_t box2);
 
 // ---------------------------------------------------------------- routing
+// Top-k over the (K-split) router logits; n_groups > topk_groups restricts the
+// selection to the topk_groups groups of E/n_groups experts with the best
+// maximum logit (n_groups <= 32); n_groups = 0 means no grouping.
 cudaError_t launch_topk(const float* partials, int ksplit, const float* bias, int T, int E, int k,
-                        float* logits_out, int32_t* topk_idx, float* topk_w, const DevStatus& st,
-                        cudaStream_t stream);
+                        float* logits_out, int32_t* topk_idx, float* topk_w, int n_groups, int topk_groups,
+                        const DevStatus& st, cudaStream_t stream);
 
 // ---------------------------------------------------------------- dispatch / histogram
 struct DispatchArgs {

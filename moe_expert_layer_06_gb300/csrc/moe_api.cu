@@ -199,9 +199,9 @@ static size_t route_ws(const moe_shape_t* s, int T) {
     return align256((size_t)p.ksplit * T * s->n_experts * sizeof(float));
 }
 
-static int route_impl(const moe_shape_t* s, int T, const void* x, const void* w_router, const float* bias,
-                      const float* logits_in, float* logits_out, int32_t* topk_idx, float* topk_w, void* ws,
-                      size_t ws_bytes, cudaStream_t stream) {
+static int route_impl(const moe_shape_t* s, int T, int n_groups, int topk_groups, const void* x,
+                      const void* w_router, const float* bias, const float* logits_in, float* logits_out,
+                      int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, cudaStream_t stream) {
     NEED4(topk_idx, "topk_idx");
     NEED4(topk_w, "topk_w");
     if (logits_out) NEED4(logits_out, "logits_out");
@@ -220,8 +220,8 @@ static int route_impl(const moe_shape_t* s, int T, const void* x, const void* w_
     int rc = device_status(&st);
     if (rc) return rc;
     if (logits_in) {
-        MOE_CUDA(launch_topk(logits_in, 1, nullptr, T, s->n_experts, s->top_k, logits_out, topk_idx, topk_w, st,
-                             stream),
+        MOE_CUDA(launch_topk(logits_in, 1, nullptr, T, s->n_experts, s->top_k, logits_out, topk_idx, topk_w,
+                             n_groups, topk_groups, st, stream),
                  "topk launch");
         return MOE_OK;
     }
@@ -244,7 +244,7 @@ static int route_impl(const moe_shape_t* s, int T, const void* x, const void* w_
     const int items = p.tiles * p.ksplit;
     MOE_CUDA(launch_gemm(kRouter, p.bn, g, std::min(items, num_sms()), stream), "router gemm launch");
     MOE_CUDA(launch_topk(static_cast<const float*>(ws), p.ksplit, bias, T, s->n_experts, s->top_k, logits_out,
-                         topk_idx, topk_w, st, stream),
+                         topk_idx, topk_w, n_groups, topk_groups, st, stream),
              "topk launch");
     return MOE_OK;
 }
@@ -518,8 +518,24 @@ int moe_route(const moe_shape_t* shape, int T, const void* x, const void* w_rout
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (T == 0) return MOE_OK;
-    return route_impl(shape, T, x, w_router, bias, logits_in, logits_out, topk_idx, topk_w, ws, ws_bytes,
+    return route_impl(shape, T, 0, 0, x, w_router, bias, logits_in, logits_out, topk_idx, topk_w, ws, ws_bytes,
                       as_stream(stream));
+}
+
+int moe_route_grouped(const moe_shape_t* shape, int T, int n_groups, int topk_groups, const void* x,
+                      const void* w_router, const float* bias, const float* logits_in, float* logits_out,
+                      int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_shape(shape, T);
+    if (rc) return rc;
+    if (n_groups < 1 || n_groups > 32 || shape->n_experts % n_groups)
+        return fail(MOE_ERR_INVALID_ARG, "n_groups %d must divide n_experts and be in [1, 32]", n_groups);
+    if (topk_groups < 1 || topk_groups > n_groups)
+        return fail(MOE_ERR_INVALID_ARG, "topk_groups %d not in [1, n_groups]", topk_groups);
+    if ((int64_t)topk_groups * (shape->n_experts / n_groups) < shape->top_k)
+        return fail(MOE_ERR_INVALID_ARG, "top_k %d exceeds the experts of %d groups", shape->top_k, topk_groups);
+    if (T == 0) return MOE_OK;
+    return route_impl(shape, T, n_groups, topk_groups, x, w_router, bias, logits_in, logits_out, topk_idx, topk_w,
+                      ws, ws_bytes, as_stream(stream));
 }
 
 int moe_expert_histogram(const moe_shape_t* shape, int T, const int32_t* topk_idx, const int32_t* replica_of,

@@ -42,7 +42,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
                                                    const float* __restrict__ bias, int T, int E, int k,
                                                    float* __restrict__ logits_out,
                                                    int32_t* __restrict__ topk_idx,
-                                                   float* __restrict__ topk_w, int tpc) {
+                                                   float* __restrict__ topk_w, int tpc, int n_groups,
+                                                   int topk_groups) {
     __shared__ float lg[kTokPerCta][EPL * 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -86,6 +87,38 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
             const float inv_den = 1.0f / den;
 
             uint32_t avail = valid;
+            if (topk_groups < n_groups) {
+                // group-limited routing: keep the topk_groups groups with the best
+                // maximum logit (ties -> lower group), then select experts in them
+                const int gs = E / n_groups;
+                float gv = -INFINITY;
+                int gi = 0x7fffffff;
+                if (lane < n_groups) {
+                    gv = lg[warp][lane * gs];
+                    for (int e = lane * gs + 1; e < (lane + 1) * gs; ++e) gv = fmaxf(gv, lg[warp][e]);
+                    gi = lane;
+                }
+                uint32_t kept = 0;
+                for (int r = 0; r < topk_groups; ++r) {
+                    float bv = (kept >> lane) & 1u ? -INFINITY : gv;
+                    int bi = (kept >> lane) & 1u ? 0x7fffffff : gi;
+#pragma unroll
+                    for (int d = 16; d > 0; d >>= 1) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+                        const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+                        if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
+                            bv = ov;
+                            bi = oi;
+                        }
+                    }
+                    kept |= 1u << bi;
+                }
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) {
+                    const int e = i * 32 + lane;
+                    if (e < E && !((kept >> (e / gs)) & 1u)) avail &= ~(1u << i);
+                }
+            }
             for (int j = 0; j < k; ++j) {
                 float bv = -INFINITY;
                 int bi = 0x7fffffff;
@@ -121,7 +154,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
 
 template <int EPL>
 cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int T, int E, int k,
-                       float* logits_out, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
+                       float* logits_out, int32_t* topk_idx, float* topk_w, int n_groups, int topk_groups,
+                       cudaStream_t stream) {
     const int threads = 256;
     const int tpc = T <= 4 * num_sms() ? 1 : kTokPerCta;
     int blocks = (T + tpc - 1) / tpc;
@@ -129,23 +163,24 @@ cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     topk_kernel<EPL><<<blocks, threads, 0, stream>>>(partials, ksplit, bias, T, E, k, logits_out, topk_idx,
-                                                     topk_w, tpc);
+                                                     topk_w, tpc, n_groups, topk_groups);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const float* partials, int ksplit, const float* bias, int T, int E, int k,
-                        float* logits_out, int32_t* topk_idx, float* topk_w, const DevStatus& st,
-                        cudaStream_t stream) {
+                        float* logits_out, int32_t* topk_idx, float* topk_w, int n_groups, int topk_groups,
+                        const DevStatus& st, cudaStream_t stream) {
     (void)st;
+    if (n_groups <= 0) n_groups = topk_groups = 1;
     const int epl = (E + 31) / 32;
-    if (epl <= 1) return launch_epl<1>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, stream);
-    if (epl <= 2) return launch_epl<2>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, stream);
-    if (epl <= 4) return launch_epl<4>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, stream);
-    if (epl <= 8) return launch_epl<8>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, stream);
-    if (epl <= 16) return launch_epl<16>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, stream);
-    if (epl <= 32) return launch_epl<32>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, stream);
+    if (epl <= 1) return launch_epl<1>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, n_groups, topk_groups, stream);
+    if (epl <= 2) return launch_epl<2>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, n_groups, topk_groups, stream);
+    if (epl <= 4) return launch_epl<4>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, n_groups, topk_groups, stream);
+    if (epl <= 8) return launch_epl<8>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, n_groups, topk_groups, stream);
+    if (epl <= 16) return launch_epl<16>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, n_groups, topk_groups, stream);
+    if (epl <= 32) return launch_epl<32>(partials, ksplit, bias, T, E, k, logits_out, topk_idx, topk_w, n_groups, topk_groups, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -133,3 +133,17 @@ def test_replica_plan_agrees_with_oracle():
     assert list(got) == [5, -1, 8, -1, -1, -1, 2, -1]
     with pytest.raises(m.MoeError):
         m.moe_eplb_plan_replicas(tiny, np.zeros(8), 5)
+
+
+def test_grouped_route_argument_checks():
+    L = m.lib()
+    s = _shape()  # E = 256, k = 8
+    b = ctypes.c_void_p(FAKE)
+    for G, Gk in ((0, 1), (33, 1), (3, 1), (8, 0), (8, 9), (64, 1)):
+        rc = L.moe_route_grouped(ctypes.byref(s), 4, G, Gk, b, b, None, None, None, b, b, b, 1 << 30, None)
+        assert rc == m.MOE_ERR_INVALID_ARG, (G, Gk)
+    s2 = _shape(n_experts=32, n_slots=32, top_k=8)  # groups of 4: k=8 needs 2 groups
+    rc = L.moe_route_grouped(ctypes.byref(s2), 4, 8, 1, b, b, None, None, None, b, b, b, 1 << 30, None)
+    assert rc == m.MOE_ERR_INVALID_ARG and "top_k" in m.last_error()
+    assert L.moe_route_grouped(ctypes.byref(s), 0, 8, 4, None, None, None, None, None, None, None, None, 0,
+                               None) == m.MOE_OK

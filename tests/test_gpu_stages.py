@@ -255,3 +255,95 @@ def test_combine_matches_oracle(name):
     assert m.moe_check_status() == 0
     ref = oracle.combine(w, T, y.double().numpy(), inv, wt32.astype(np.float64), ysh.double().numpy())
     assert_close(to_np(out), ref, what="combine")
+
+
+# ----------------------------------------------------------------------------- group-limited routing
+
+GROUPED = [("tiny", 4, 2), ("mid", 4, 2), ("deep", 2, 1), ("decode_t32", 8, 4), ("decode_t256_skew", 8, 2),
+           ("prefill_t4096", 8, 3)]
+
+
+@pytest.mark.parametrize("name,G,Gk", GROUPED)
+def test_grouped_topk_from_fp32_logits_is_bit_exact(name, G, Gk):
+    w = _wl(name)
+    T, k = w.tokens, w.top_k
+    lg = mi.fp32_logits(w)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    m.moe_route_grouped(w, T, G, Gk, None, None, None, lg.to(DEV), None, idx, tw, None)
+    assert m.moe_check_status() == 0
+    idx_o, wt_o = oracle.topk_grouped(lg.double(), k, G, Gk)
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    np.testing.assert_allclose(tw.cpu().numpy(), wt_o, rtol=2e-6, atol=1e-9)
+    gs = w.n_experts // G
+    assert all(len({int(e) // gs for e in row}) <= Gk for row in idx_o)
+
+
+def _grouped_sure(lo, k, G, Gk, gap=1e-4):
+    """Tokens whose group choice and expert choice are both decided by more than gap."""
+    T, E = lo.shape
+    gmax = -np.sort(-lo.reshape(T, G, E // G).max(axis=2), axis=1)
+    g_ok = (gmax[:, Gk - 1] - gmax[:, Gk]) > gap if Gk < G else np.ones(T, bool)
+    idx, _ = oracle.topk_grouped(lo, k, G, Gk)
+    masked = np.full_like(lo, -np.inf)
+    for t in range(T):
+        keep = sorted({int(e) // (E // G) for e in idx[t]} |
+                      set(np.argsort(-lo[t].reshape(G, E // G).max(axis=1), kind="stable")[:Gk].tolist()))
+        for g in keep:
+            masked[t, g * (E // G):(g + 1) * (E // G)] = lo[t, g * (E // G):(g + 1) * (E // G)]
+    s = -np.sort(-masked, axis=1)
+    e_ok = (s[:, k - 1] - s[:, k]) > gap if s.shape[1] > k else np.ones(T, bool)
+    return g_ok & e_ok, idx
+
+
+@pytest.mark.parametrize("name,G,Gk", [("mid", 4, 2), ("decode_t32", 8, 4), ("prefill_t4096", 8, 3)])
+def test_grouped_routing_from_router_gemm(name, G, Gk):
+    w = _wl(name)
+    T, k = w.tokens, w.top_k
+    from moe_testlib import parallel_router_logits
+    x, wr = mi.hidden_states(w), mi.router_weight(w)
+    lo_o = parallel_router_logits(w, x, wr, None)
+    sure, idx_o = _grouped_sure(lo_o, k, G, Gk)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(1, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=DEV)
+    m.moe_route_grouped(w, T, G, Gk, x.to(DEV), wr.to(DEV), None, None, None, idx, tw, ws)
+    assert m.moe_check_status() == 0
+    got = np.sort(idx.cpu().numpy(), 1)
+    assert sure.mean() > 0.9
+    assert np.array_equal(got[sure], np.sort(idx_o, 1)[sure])
+
+
+def test_grouped_routing_layer_matches_oracle():
+    """Staged layer (grouped route, dispatch, FFN, combine) against the oracle's pieces."""
+    w = MID
+    G, Gk = 4, 2
+    T, k, H = w.tokens, w.top_k, w.hidden
+    x, wr = mi.hidden_states(w), mi.router_weight(w)
+    wg, wu, wd = mi.stacked_expert_weights(w)
+    sg, su, sd = mi.stacked_shared_weights(w)
+    lo = oracle.router_logits(w, x, wr, None)
+    sure, _ = _grouped_sure(lo, k, G, Gk)
+    idx_o, wt_o = oracle.topk_grouped(lo, k, G, Gk)
+    so, _ = oracle.slot_map(w, idx_o)
+    cnt, _ = oracle.histogram(w, so)
+    off, perm, inv, xd = oracle.dispatch(w, T, so, cnt, x)
+    y_o = oracle.expert_ffn(w, T, off, xd, wg, wu, wd)
+    ref = oracle.combine(w, T, y_o, inv, wt_o, oracle.shared_rows(w, x, sg, su, sd))
+    d = dict(x=x.to(DEV), wr=wr.to(DEV), wg=wg.to(DEV), wu=wu.to(DEV), wd=wd.to(DEV), sg=sg.to(DEV),
+             su=su.to(DEV), sd=sd.to(DEV))
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(1, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=DEV)
+    m.moe_route_grouped(w, T, G, Gk, d["x"], d["wr"], None, None, None, idx, tw, ws)
+    g = _gpu_dispatch(w, d["x"], idx.cpu().numpy(), None)
+    y = torch.empty((T * k, H), dtype=torch.bfloat16, device=DEV)
+    ysh = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    fws = torch.empty(m.moe_ffn_workspace_size(w, T), dtype=torch.uint8, device=DEV)
+    m.moe_expert_ffn(w, T, d["x"], g["x_disp"], g["offsets"], d["wg"], d["wu"], d["wd"], d["sg"], d["su"], d["sd"],
+                     y, ysh, m.MOE_FFN_AUTO, fws)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    m.moe_combine(w, T, y, g["inv"], tw, ysh, out)
+    assert m.moe_check_status() == 0
+    assert np.array_equal(np.sort(idx.cpu().numpy(), 1)[sure], np.sort(idx_o, 1)[sure])
+    assert_close(to_np(out)[sure], ref[sure], what="grouped layer")
