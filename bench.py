@@ -188,8 +188,15 @@ def run_ours(args, rank, world, local_rank):
     rws = torch.empty(max(16, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    groups = None
+    if args.route_groups:
+        groups = tuple(int(v) for v in args.route_groups.split(":"))
+
     def step(ev=None):
-        m.moe_route(w, T, x, wr, bias, None, None, idx, tw, rws)
+        if groups:
+            m.moe_route_grouped(w, T, groups[0], groups[1], x, wr, bias, None, None, idx, tw, rws)
+        else:
+            m.moe_route(w, T, x, wr, bias, None, None, idx, tw, rws)
         m.moe_dispatch(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x_disp)
         if ev is not None:
             ev[0].record(stream)
@@ -243,7 +250,11 @@ def run_ours(args, rank, world, local_rank):
 
     def e2e_step():
         x_e2e.copy_(x_host, non_blocking=True)
-        m.moe_forward(w, T, x_e2e, wr, bias, repd, wg, wu, wd, sg, su, sd, out, ws=ws)
+        if groups:  # the whole layer through the staged calls (moe_forward routes over all experts)
+            x.copy_(x_e2e)
+            step()
+        else:
+            m.moe_forward(w, T, x_e2e, wr, bias, repd, wg, wu, wd, sg, su, sd, out, ws=ws)
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -294,6 +305,7 @@ def run_ours(args, rank, world, local_rank):
             "touched_slots": bf["touched"],
             "l2": "inputs larger than L2: each step streams %.1f GB of touched expert weights" % (bf["bytes"] / 1e9),
             "parallelism": "replica x%d (independent layer per GPU)" % world,
+            "routing": ("group-limited: %d groups, keep %d" % groups) if groups else "top-%d of all experts" % k,
         },
         "us_per_layer": round(ms_step * 1e3, 2),
         "layer_roofline": {
@@ -430,6 +442,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--route-groups", default="", help="G:Gk group-limited routing (timed region only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
