@@ -243,3 +243,19 @@ def plan_replicas(w, expert_counts, n_rep: int) -> np.ndarray:
     if rc != 0:
         raise ValueError("replica plan does not fit the shape")
     return rep
+
+
+def eplb_window(w, history, window: int, replica_of=None, threshold: float = 1.2):
+    """Sliding-window monitor: returns slot_window, block_load, expert_load, ratio, trigger."""
+    h = np.ascontiguousarray(history, dtype=np.int32)
+    n = h.shape[0]
+    assert h.shape[1] == w.n_slots + 1
+    sw = np.empty(w.n_slots + 1, np.int64)
+    bl = np.empty(w.n_blocks, np.int64)
+    el = np.empty(w.n_experts, np.int64)
+    ratio = ctypes.c_double()
+    trig = ctypes.c_int()
+    lib().oracle_eplb_window(ctypes.byref(shape_of(w)), n, _ptr(h), window, _ptr(_i32(replica_of)),
+                             ctypes.c_double(threshold), _ptr(sw), _ptr(bl), _ptr(el), ctypes.byref(ratio),
+                             ctypes.byref(trig))
+    return sw, bl, el, ratio.value, bool(trig.value)

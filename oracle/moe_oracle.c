@@ -390,3 +390,33 @@ int oracle_plan_replicas(const oracle_shape* s, const int32_t* counts, int n_rep
     free(used);
     return rc;
 }
+
+/* Section 6.2, monitor (arrival counts over a recent window, per-rank sums) and
+ * detect (max/mean rank load against a threshold).  Readings in the header. */
+void oracle_eplb_window(const oracle_shape* s, int n_batches, const int32_t* history, int window,
+                        const int32_t* replica_of, double threshold, int64_t* slot_window,
+                        int64_t* block_load, int64_t* expert_load, double* ratio, int* trigger) {
+    const int S = s->n_slots, B = s->n_blocks, E = s->n_experts;
+    const int spb = S / B;
+    const int first = n_batches > window ? n_batches - window : 0;
+    for (int i = 0; i <= S; ++i) {
+        int64_t acc = 0;
+        for (int b = first; b < n_batches; ++b) acc += history[(size_t)b * (S + 1) + i];
+        slot_window[i] = acc;
+    }
+    int64_t mx = 0, total = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t acc = 0;
+        for (int i = b * spb; i < (b + 1) * spb; ++i) acc += slot_window[i];
+        block_load[b] = acc;
+        total += acc;
+        if (acc > mx) mx = acc;
+    }
+    for (int e = 0; e < E; ++e) {
+        int64_t acc = slot_window[oracle_home_slot(s, e)];
+        if (replica_of && replica_of[e] >= 0) acc += slot_window[replica_of[e]];
+        expert_load[e] = acc;
+    }
+    *ratio = total > 0 ? (double)mx * (double)B / (double)total : 0.0;
+    *trigger = (double)mx * (double)B > threshold * (double)total;
+}

@@ -126,6 +126,21 @@ void oracle_token_output(const oracle_shape* s, const uint16_t* x_row, int k,
                          const uint16_t* ws_gate, const uint16_t* ws_up, const uint16_t* ws_down,
                          double* out);
 
+/* EPLB monitor and detection over a sliding window (section 6.2: per-expert
+ * arrival rates over a recent window, per-rank load = sum over its experts,
+ * rebalance when max/mean rank load exceeds a threshold such as 1.2).
+ * Reading: the window is the last `window` batches (not a time span).
+ * history [n_batches][S+1]: per-slot counts of each batch, oldest first.
+ * slot_window[S+1] = sum of the last min(window, n_batches) rows;
+ * block_load[B] = sum of slot_window over the block's slots;
+ * expert_load[E] = slot_window of the expert's home slot plus that of its
+ * replica slot (replica_of may be NULL);
+ * ratio = max(block_load) * B / sum(block_load) (0 when the sum is 0);
+ * trigger = max * B > threshold * sum, evaluated in double. */
+void oracle_eplb_window(const oracle_shape* s, int n_batches, const int32_t* history, int window,
+                        const int32_t* replica_of, double threshold, int64_t* slot_window,
+                        int64_t* block_load, int64_t* expert_load, double* ratio, int* trigger);
+
 /* Replica placement for n_rep redundant slots from per-expert counts[E].
  * Hot list: the n_rep experts with the largest counts (ties -> lower id).
  * Each block initially carries the load of its experts, a hot expert's

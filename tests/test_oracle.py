@@ -410,3 +410,50 @@ def test_token_output_matches_whole_layer():
         gud = [(wg[e], wu[e], wd[e]) for e in r["idx"][t]]
         y = oracle.token_output(w, x[t], r["weight"][t], gud, sg, su, sd)
         np.testing.assert_allclose(y, r["out"][t], rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------------ EPLB sliding window
+
+
+def test_eplb_window_hand_case():
+    w = _tiny(n_experts=8, n_blocks=4, n_slots=12)  # blocks of 3 slots: experts 2b, 2b+1, replica slot
+    rep = np.array([-1, -1, -1, 5, -1, -1, -1, -1], dtype=np.int32)  # expert 3 replicated in slot 5
+    h = np.zeros((3, 13), dtype=np.int32)
+    h[0, 0] = 9          # dropped by a window of 2
+    h[1, 4] = 4          # expert 3 home (slot 4)
+    h[1, 5] = 2          # expert 3 replica
+    h[2, 0] = 3
+    h[2, 10] = 1         # expert 7
+    h[2, 12] = 5         # invalid bucket: not a block's load
+    sw, bl, el, ratio, trig = oracle.eplb_window(w, h, 2, rep, 1.2)
+    assert list(sw) == [3, 0, 0, 0, 4, 2, 0, 0, 0, 0, 1, 0, 5]
+    assert list(bl) == [3, 6, 0, 1]
+    assert list(el) == [3, 0, 0, 6, 0, 0, 0, 1]
+    assert ratio == 6 * 4 / 10 and trig
+    sw, bl, _, _, _ = oracle.eplb_window(w, h, 3, rep, 1.2)
+    assert list(bl) == [12, 6, 0, 1]
+    _, _, _, ratio, trig = oracle.eplb_window(w, np.ones((1, 13), np.int32), 4, None, 1.2)
+    assert ratio == 1.0 and not trig
+    _, _, _, ratio, trig = oracle.eplb_window(w, np.zeros((2, 13), np.int32), 4, None, 1.2)
+    assert ratio == 0.0 and not trig
+
+
+def test_eplb_window_matches_histograms_of_recent_batches():
+    w = _tiny(tokens=30, n_experts=16, n_blocks=4, n_slots=16, top_k=3)
+    rng = np.random.default_rng(11)
+    hist = []
+    for _ in range(7):
+        idx = np.stack([rng.choice(16, 3, replace=False) for _ in range(w.tokens)]).astype(np.int32)
+        so, _ = oracle.slot_map(w, idx)
+        c, _ = oracle.histogram(w, so)
+        hist.append(c)
+    hist = np.array(hist)
+    for window in (1, 3, 7, 10):
+        sw, bl, el, ratio, _ = oracle.eplb_window(w, hist, window)
+        recent = hist[-window:].sum(axis=0)
+        assert np.array_equal(sw, recent)
+        assert bl.sum() == min(window, 7) * w.tokens * w.top_k
+        assert np.array_equal(el, recent[:16])
+        assert abs(ratio - bl.max() * 4 / bl.sum()) < 1e-15
+        _, bl1, _, _, _ = oracle.eplb_window(w, hist[-1:], 1)
+        assert np.array_equal(bl1, oracle.histogram(w, oracle.slot_map(w, idx)[0])[1])

@@ -33,6 +33,12 @@ MUTANTS = [
      "if (l[e] < best) best = l[e];\n            gscore[g] = best;"),
     ("group ties go to the higher group", "if (bg < 0 || ranks_before(gscore[g], g, gscore[bg], bg)) bg = g;",
      "if (bg < 0 || ranks_before(gscore[g], -g, gscore[bg], -bg)) bg = g;"),
+    ("window keeps one batch too many", "const int first = n_batches > window ? n_batches - window : 0;",
+     "const int first = n_batches > window + 1 ? n_batches - window - 1 : 0;"),
+    ("expert load ignores its replica", "if (replica_of && replica_of[e] >= 0) acc += slot_window[replica_of[e]];",
+     "(void)replica_of;"),
+    ("trigger compares the mean", "*trigger = (double)mx * (double)B > threshold * (double)total;",
+     "*trigger = (double)total > threshold * (double)total;"),
     ("home slot ignores the replica slots", "return (e / epb) * spb + (e % epb);", "return e;"),
     ("replica used by even tokens", "replica_of[e] >= 0 && (t % 2) == 1", "replica_of[e] >= 0 && (t % 2) == 0"),
     ("dispatch fills slots in reverse order", "for (int a = 0; a < n; ++a) {\n        const int32_t slot = slot_of[a];",
@@ -73,6 +79,8 @@ PINS = [
     pins.test_replica_plan_hot_list_ties_go_to_lower_id,
     pins.test_replica_plan_falls_back_to_home_block,
     pins.test_replicated_layer_equals_plain_layer_exactly,
+    pins.test_eplb_window_hand_case,
+    pins.test_eplb_window_matches_histograms_of_recent_batches,
 ]
 
 
