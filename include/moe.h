@@ -168,6 +168,52 @@ MOE_API double moe_eplb_imbalance(const int32_t* host_block_counts, int n_blocks
 MOE_API int moe_eplb_plan_replicas(const moe_shape_t* shape, const int32_t* host_expert_counts, int n_rep,
                            int32_t* host_replica_of);
 
+/* ---------------------------------------------------------------- EPLB online loop
+ * Section 6.2: monitor arrivals over a recent window, detect when the most
+ * loaded rank exceeds the mean by a threshold (1.2 in the post), copy hot
+ * experts to other ranks and switch the routing table without stopping
+ * inference.  The window is the last `window` batches (a reading: the post
+ * speaks of a time span such as 100 ms).
+ *
+ * moe_eplb_window_bytes / _reset: size and zeroing of the caller-owned device
+ * state (ring of `window` rows of S+1 int32 slot counts + S+1 int64 sums).
+ * moe_eplb_window_push: one small kernel per batch, no host synchronisation.
+ * Pushes counts [S+1] (as written by moe_dispatch / moe_expert_histogram),
+ * dropping the oldest row once full, then writes (each output may be NULL,
+ * all device pointers):
+ *   block_load[B]  = windowed counts summed over the block's slots (int64);
+ *   expert_load[E] = windowed count of e's home slot + its replica slot under
+ *                    replica_of (may be NULL) (int64);
+ *   ratio[1]       = max(block_load) * B / sum(block_load), 0 if the sum is 0;
+ *   trigger[1]     = 1 if max * B > threshold * sum (evaluated in double).
+ * Calls on one state must be stream-ordered. */
+MOE_API size_t moe_eplb_window_bytes(const moe_shape_t* shape, int window);
+MOE_API int moe_eplb_window_reset(const moe_shape_t* shape, int window, void* state, size_t state_bytes,
+                                  void* stream);
+MOE_API int moe_eplb_window_push(const moe_shape_t* shape, int window, void* state, size_t state_bytes,
+                                 const int32_t* counts, const int32_t* replica_of, double threshold,
+                                 int64_t* block_load, int64_t* expert_load, double* ratio, int32_t* trigger,
+                                 void* stream);
+
+/* Migration without stopping inference (host helpers, RCU-like switch).
+ * A new plan (moe_eplb_plan_replicas) overwrites replica slots that the old
+ * plan may still be using.  Safe order on one device:
+ *   1. moe_eplb_stable_table(old, new, stable): stable[e] = old[e] where the
+ *      old and new plans agree, else -1 (home slot only); upload it and use it
+ *      for every batch enqueued from now on;
+ *   2. on a copy stream that waits for the last batch using `old`, call
+ *      moe_eplb_copy_replicas(old, new, ...): for every expert whose replica
+ *      slot changes, 3 device-to-device copies (gate, up, down) from its home
+ *      slot into the new replica slot (no allocation);
+ *   3. make the compute stream wait for the copies, then use `new`.
+ * Every batch sees a table whose replica slots hold the right weights, so the
+ * layer output is unchanged throughout (replicas are byte copies).  host_old
+ * may be NULL (no replicas before).  Weights are slot-major [S,I,H] / [S,H,I]. */
+MOE_API int moe_eplb_stable_table(const moe_shape_t* shape, const int32_t* host_old, const int32_t* host_new,
+                                  int32_t* host_out);
+MOE_API int moe_eplb_copy_replicas(const moe_shape_t* shape, const int32_t* host_old, const int32_t* host_new,
+                                   void* w_gate, void* w_up, void* w_down, void* stream);
+
 /* ---------------------------------------------------------------- step 2: dispatch
  * Section 2.2 step 2.  Slot map and histogram as moe_expert_histogram, then
  *   offsets[s] = sum_{s'<s} counts[s'] for s <= S+1 (offsets[S+1] = T*k; the

@@ -36,6 +36,8 @@ EXPORTS = (
     "moe_eplb_imbalance", "moe_eplb_plan_replicas", "moe_dispatch", "moe_expert_gate_up",
     "moe_expert_down", "moe_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
     "moe_workspace_size", "moe_forward", "moe_expert_ffn_noalloc", "moe_route_grouped",
+    "moe_eplb_window_bytes", "moe_eplb_window_reset", "moe_eplb_window_push", "moe_eplb_stable_table",
+    "moe_eplb_copy_replicas",
 )
 
 # capacity of the fixed scratch of moe_expert_ffn_noalloc (include/moe.h)
@@ -74,6 +76,11 @@ _SIG = {
     "moe_route_grouped": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_histogram": (_I, [_P, _I, _P, _P, _P, _P, _P]),
     "moe_eplb_imbalance": (ctypes.c_double, [_P, _I]),
+    "moe_eplb_window_bytes": (_Z, [_P, _I]),
+    "moe_eplb_window_reset": (_I, [_P, _I, _P, _Z, _P]),
+    "moe_eplb_window_push": (_I, [_P, _I, _P, _Z, _P, _P, ctypes.c_double, _P, _P, _P, _P, _P]),
+    "moe_eplb_stable_table": (_I, [_P, _P, _P, _P]),
+    "moe_eplb_copy_replicas": (_I, [_P, _P, _P, _P, _P, _P, _P]),
     "moe_eplb_plan_replicas": (_I, [_P, _P, _I, _P]),
     "moe_dispatch": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_gate_up": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
@@ -192,6 +199,40 @@ def moe_eplb_plan_replicas(shape, expert_counts, n_rep: int):
     out = np.empty(shape.n_experts, dtype=np.int32)
     _check(lib().moe_eplb_plan_replicas(_shape(shape), c.ctypes.data, n_rep, out.ctypes.data))
     return out
+
+
+def moe_eplb_window_bytes(shape, window: int) -> int:
+    return lib().moe_eplb_window_bytes(_shape(shape), window)
+
+
+def moe_eplb_window_reset(shape, window, state, stream=None):
+    _check(lib().moe_eplb_window_reset(_shape(shape), window, _ptr(state), state.numel() * state.element_size(),
+                                       _stream(stream)))
+
+
+def moe_eplb_window_push(shape, window, state, counts, replica_of=None, threshold=1.2, block_load=None,
+                         expert_load=None, ratio=None, trigger=None, stream=None):
+    _check(lib().moe_eplb_window_push(_shape(shape), window, _ptr(state), state.numel() * state.element_size(),
+                                      _ptr(counts), _ptr(replica_of), float(threshold), _ptr(block_load),
+                                      _ptr(expert_load), _ptr(ratio), _ptr(trigger), _stream(stream)))
+
+
+def moe_eplb_stable_table(shape, old, new):
+    import numpy as np
+    o = np.ascontiguousarray(old, dtype=np.int32) if old is not None else None
+    n = np.ascontiguousarray(new, dtype=np.int32)
+    out = np.empty(shape.n_experts, dtype=np.int32)
+    _check(lib().moe_eplb_stable_table(_shape(shape), o.ctypes.data if o is not None else None, n.ctypes.data,
+                                       out.ctypes.data))
+    return out
+
+
+def moe_eplb_copy_replicas(shape, old, new, w_gate, w_up, w_down, stream=None):
+    import numpy as np
+    o = np.ascontiguousarray(old, dtype=np.int32) if old is not None else None
+    n = np.ascontiguousarray(new, dtype=np.int32)
+    _check(lib().moe_eplb_copy_replicas(_shape(shape), o.ctypes.data if o is not None else None, n.ctypes.data,
+                                        _ptr(w_gate), _ptr(w_up), _ptr(w_down), _stream(stream)))
 
 
 def moe_dispatch(shape, T, x, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm,

@@ -147,3 +147,39 @@ def test_grouped_route_argument_checks():
     assert rc == m.MOE_ERR_INVALID_ARG and "top_k" in m.last_error()
     assert L.moe_route_grouped(ctypes.byref(s), 0, 8, 4, None, None, None, None, None, None, None, None, 0,
                                None) == m.MOE_OK
+
+
+def test_eplb_window_and_migration_argument_checks():
+    L = m.lib()
+    w = mi.WORKLOADS["redundant_t1024"]
+    s = _shape(n_slots=264)
+    b = ctypes.c_void_p(FAKE)
+    n1 = L.moe_eplb_window_bytes(ctypes.byref(s), 1)
+    n4 = L.moe_eplb_window_bytes(ctypes.byref(s), 4)
+    assert n1 > 0 and n4 - n1 >= 3 * 265 * 4 - 16 and L.moe_eplb_window_bytes(ctypes.byref(s), 0) == 0
+    assert L.moe_eplb_window_reset(ctypes.byref(s), 0, b, n4, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_eplb_window_reset(ctypes.byref(s), 4, None, n4, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_eplb_window_reset(ctypes.byref(s), 4, b, n4 - 1, None) == m.MOE_ERR_WORKSPACE
+    push = lambda win, st, nb, cnt, thr: L.moe_eplb_window_push(ctypes.byref(s), win, st, nb, cnt, None, thr,
+                                                                None, None, None, None, None)
+    assert push(4, b, n4, None, 1.2) == m.MOE_ERR_INVALID_ARG
+    assert push(4, b, n4, b, 0.0) == m.MOE_ERR_INVALID_ARG
+    assert push(4, b, n1, b, 1.2) == m.MOE_ERR_WORKSPACE
+    assert push(4, ctypes.c_void_p(FAKE + 4), n4, b, 1.2) == m.MOE_ERR_INVALID_ARG
+    # stable table: keep replicas both plans agree on
+    old = np.full(256, -1, np.int32)
+    new = np.full(256, -1, np.int32)
+    old[[3, 40, 77]] = [65, 98, 131]
+    new[[3, 40, 90]] = [65, 131, 98]
+    st = m.moe_eplb_stable_table(w, old, new)
+    assert list(np.flatnonzero(st >= 0)) == [3] and st[3] == 65
+    assert list(m.moe_eplb_stable_table(w, None, new)) == [-1] * 256
+    # copies are validated before anything is enqueued
+    bad = new.copy()
+    bad[5] = 34   # a home slot (block 1 holds experts 32..63 in slots 33..64)
+    with pytest.raises(m.MoeError):
+        m.moe_eplb_copy_replicas(w, old, bad, FAKE, FAKE, FAKE)
+    dup = new.copy()
+    dup[7] = 65
+    with pytest.raises(m.MoeError):
+        m.moe_eplb_copy_replicas(w, old, dup, FAKE, FAKE, FAKE)
