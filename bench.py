@@ -433,6 +433,102 @@ def run_reference(args, rank, world):
     }
 
 
+def run_eplb(args):
+    """Cost of the online EPLB loop on the redundant-expert workload (one JSON line).
+
+    Times the layer alone, the layer plus the sliding-window push after every
+    batch, and a full replica migration (all replica slots re-planned) copied
+    on a side stream while the compute stream keeps serving with the stable
+    table.
+    """
+    import moe_expert_layer_06_gb300 as m
+    m.build_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = mi.WORKLOADS["redundant_t1024"] if args.config == DEFAULT_CONFIG else mi.WORKLOADS[args.config]
+    assert w.n_slots > w.n_experts, "the EPLB mode needs a workload with replica slots"
+    T, window = w.tokens, 8
+    plan_a = replica_plan_gpu(m, w, dev)
+    plan_b = m.moe_eplb_plan_replicas(w, np.arange(w.n_experts, dtype=np.int32)[::-1].copy(), w.n_slots - w.n_experts)
+    x = mi.hidden_states(w, device=dev)
+    wr = mi.router_weight(w, device=dev)
+    bias = torch.from_numpy(mi.router_bias(w)).to(dev) if w.skew_alpha else None
+    wg, wu, wd = mi.stacked_expert_weights(w, plan_a, device=dev)
+    sg, su, sd = mi.stacked_shared_weights(w, device=dev)
+    mi.clear_cache()
+    out = torch.empty((T, w.hidden), dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(w.n_slots + 1, dtype=torch.int32, device=dev)
+    ws = torch.empty(m.moe_workspace_size(w, T), dtype=torch.uint8, device=dev)
+    state = torch.empty(m.moe_eplb_window_bytes(w, window), dtype=torch.uint8, device=dev)
+    m.moe_eplb_window_reset(w, window, state)
+    bl = torch.empty(w.n_blocks, dtype=torch.int64, device=dev)
+    el = torch.empty(w.n_experts, dtype=torch.int64, device=dev)
+    ratio = torch.empty(1, dtype=torch.float64, device=dev)
+    trig = torch.empty(1, dtype=torch.int32, device=dev)
+    tables = {n: torch.from_numpy(np.ascontiguousarray(t, np.int32)).to(dev)
+              for n, t in (("a", plan_a), ("b", plan_b), ("stable", m.moe_eplb_stable_table(w, plan_a, plan_b)))}
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd(table):
+        m.moe_forward(w, T, x, wr, bias, tables[table], wg, wu, wd, sg, su, sd, out, counts_out=counts, ws=ws)
+
+    def push():
+        m.moe_eplb_window_push(w, window, state, counts, tables["a"], 1.2, bl, el, ratio, trig)
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    for _ in range(args.warmup):
+        fwd("a")
+        push()
+    steps = max(args.steps, 10)
+    t_plain = timed(lambda: fwd("a"), steps)
+    t_window = timed(lambda: (fwd("a"), push()), steps)
+    t_push = timed(push, steps)
+    # migration: copies on a side stream, serving continues with the stable table
+    copy = torch.cuda.Stream(device=dev)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    ready = torch.cuda.Event()
+    ready.record(stream)
+    with torch.cuda.stream(copy):
+        copy.wait_event(ready)
+        c0.record(copy)
+        m.moe_eplb_copy_replicas(w, plan_a, plan_b, wg, wu, wd, stream=copy)
+        c1.record(copy)
+    s0.record(stream)
+    fwd("stable")  # one step served concurrently with the copies
+    s1.record(stream)
+    stream.wait_event(c1)
+    fwd("b")
+    torch.cuda.synchronize(dev)
+    if m.moe_check_status() != 0:
+        raise RuntimeError(m.last_error())
+    copy_ms = c0.elapsed_time(c1)
+    changed = int(sum(1 for e in range(w.n_experts) if plan_b[e] >= 0 and plan_b[e] != plan_a[e]))
+    copy_bytes = changed * 3 * w.hidden * w.inter * 2
+    return {
+        "mode": "eplb", "metric": "online EPLB loop cost", "unit": "ms", "higher_is_better": False,
+        "config": {"workload": w.name, "tokens": T, "n_slots": w.n_slots, "window_batches": window,
+                   "threshold": 1.2, "replicas_moved": changed},
+        "ms_per_step_layer": round(t_plain, 4),
+        "ms_per_step_layer_plus_window": round(t_window, 4),
+        "window_push_us": round(t_push * 1e3, 2),
+        "migration_copy_ms": round(copy_ms, 3),
+        "migration_copy_gbs": round(2 * copy_bytes / (copy_ms * 1e-3) / 1e9, 1),
+        "ms_one_step_concurrent_with_copy": round(s0.elapsed_time(s1), 4),
+        "imbalance_ratio": round(float(ratio.item()), 4), "trigger": int(trig.item()),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,12 +539,16 @@ def main():
     ap.add_argument("--cpu-sample", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--route-groups", default="", help="G:Gk group-limited routing (timed region only)")
+    ap.add_argument("--eplb", action="store_true", help="time the online EPLB loop instead (own JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.eplb:
+        print(json.dumps(run_eplb(args)), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
