@@ -259,3 +259,57 @@ def eplb_window(w, history, window: int, replica_of=None, threshold: float = 1.2
                              ctypes.c_double(threshold), _ptr(sw), _ptr(bl), _ptr(el), ctypes.byref(ratio),
                              ctypes.byref(trig))
     return sw, bl, el, ratio.value, bool(trig.value)
+
+
+# ------------------------------------------------------------------ FP8
+
+def e4m3_encode(values) -> np.ndarray:
+    f = lib().oracle_e4m3_encode
+    f.restype = ctypes.c_uint8
+    f.argtypes = [ctypes.c_float]
+    v = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([f(float(a)) for a in v], dtype=np.uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    f = lib().oracle_e4m3_decode
+    f.restype = ctypes.c_double
+    f.argtypes = [ctypes.c_uint8]
+    return np.array([f(int(c)) for c in np.asarray(codes).ravel()], dtype=np.float64)
+
+
+def quantize_rows_e4m3(x):
+    """Per-row E4M3 codes [R, C] (uint8) and fp32 scales [R] of a bf16 tensor."""
+    xs = _u16(x)
+    R, C = xs.shape[0], int(np.prod(xs.shape[1:]))
+    codes = np.empty((R, C), dtype=np.uint8)
+    scale = np.empty(R, dtype=np.float32)
+    lib().oracle_quantize_rows_e4m3(R, C, _ptr(xs), _ptr(codes), _ptr(scale))
+    return codes.reshape(xs.shape), scale
+
+
+def swiglu_row_fp8(qx, sx, qg, sg, qu, su, w_down) -> np.ndarray:
+    qx, qg, qu = (np.ascontiguousarray(a, np.uint8) for a in (qx, qg, qu))
+    sg, su = _f32(sg), _f32(su)
+    d = _u16(w_down)
+    I, H = qg.shape
+    y = np.empty(H, dtype=np.float64)
+    lib().oracle_swiglu_row_fp8(H, I, _ptr(qx), ctypes.c_float(float(sx)), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su),
+                                _ptr(d), _ptr(y))
+    return y
+
+
+def moe_forward_fp8(w, x, w_router, bias, replica_of, q, ws_down_bf16):
+    """Layer with FP8 payload and FP8 gate/up; q = dict(qg, sg, qu, su, wd, qsg, ssg, qsu, ssu)."""
+    T = x.shape[0]
+    idx = np.empty((T, w.top_k), np.int32)
+    out = np.empty((T, w.hidden), np.float64)
+    arr = [np.ascontiguousarray(q[k], np.uint8 if k.startswith("q") else np.float32)
+           for k in ("qg", "sg", "qu", "su")]
+    sh = [np.ascontiguousarray(q[k], np.uint8 if k.startswith("q") else np.float32)
+          for k in ("qsg", "ssg", "qsu", "ssu")]
+    inv = lib().oracle_moe_forward_fp8(
+        ctypes.byref(shape_of(w)), T, _ptr(_u16(x)), _ptr(_u16(w_router)), _ptr(_f32(bias)),
+        _ptr(_i32(replica_of)), _ptr(arr[0]), _ptr(arr[1]), _ptr(arr[2]), _ptr(arr[3]), _ptr(_u16(q["wd"])),
+        _ptr(sh[0]), _ptr(sh[1]), _ptr(sh[2]), _ptr(sh[3]), _ptr(_u16(ws_down_bf16)), _ptr(idx), _ptr(out))
+    return dict(idx=idx, out=out, invalid=inv)

@@ -420,3 +420,118 @@ void oracle_eplb_window(const oracle_shape* s, int n_batches, const int32_t* his
     *ratio = total > 0 ? (double)mx * (double)B / (double)total : 0.0;
     *trigger = (double)mx * (double)B > threshold * (double)total;
 }
+
+/* ---- FP8.  Section 2.3: FP8 communication halves the dispatch + combine
+ * volume.  Format: OCP 8-bit floating point E4M3 (definition in the header). */
+uint8_t oracle_e4m3_encode(float v) {
+    if (isnan(v)) return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;  /* saturate */
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal grid: multiples of 2^-9; rounding up to 8 * 2^-9 gives the
+         * smallest normal, whose code is 8 as well */
+        const double m = rint(a * ldexp(1.0, 9)); /* default mode: nearest, ties to even */
+        return sign | (uint8_t)m;
+    }
+    int ex;
+    frexp(a, &ex);              /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;             /* a in [2^e, 2^(e+1)) */
+    double m = rint((a * ldexp(1.0, -e) - 1.0) * 8.0);
+    if (m == 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    return sign | (uint8_t)(((e + 7) << 3) | (int)m);
+}
+
+double oracle_e4m3_decode(uint8_t code) {
+    const int e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return (code & 0x80) ? -mag : mag;
+}
+
+void oracle_quantize_rows_e4m3(int rows, int cols, const uint16_t* x_bf16, uint8_t* codes, float* scale) {
+    for (int r = 0; r < rows; ++r) {
+        float amax = 0.0f;
+        for (int c = 0; c < cols; ++c) {
+            const float v = fabsf((float)oracle_bf16_to_double(x_bf16[(size_t)r * cols + c]));
+            if (v > amax) amax = v;
+        }
+        const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[r] = s;
+        for (int c = 0; c < cols; ++c)
+            codes[(size_t)r * cols + c] = oracle_e4m3_encode((float)oracle_bf16_to_double(x_bf16[(size_t)r * cols + c]) / s);
+    }
+}
+
+void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
+                           const uint8_t* qu, const float* su, const uint16_t* w_down, double* y) {
+    double* h = (double*)malloc((size_t)I * sizeof(double));
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < H; ++c) {
+            const double xv = oracle_e4m3_decode(qx[c]);
+            g += xv * oracle_e4m3_decode(qg[(size_t)i * H + c]);
+            u += xv * oracle_e4m3_decode(qu[(size_t)i * H + c]);
+        }
+        g *= (double)sx * (double)sg[i];
+        u *= (double)sx * (double)su[i];
+        h[i] = silu(g) * u;
+    }
+    for (int o = 0; o < H; ++o) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += h[i] * oracle_bf16_to_double(w_down[(size_t)o * I + i]);
+        y[o] = acc;
+    }
+    free(h);
+}
+
+int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
+                           const float* bias, const int32_t* replica_of, const uint8_t* qg, const float* sg,
+                           const uint8_t* qu, const float* su, const uint16_t* w_down, const uint8_t* qsg,
+                           const float* ssg, const uint8_t* qsu, const float* ssu, const uint16_t* ws_down,
+                           int32_t* idx, double* out) {
+    const int H = s->hidden, E = s->n_experts, k = s->top_k, S = s->n_slots, I = s->inter;
+    const int Is = s->inter_shared;
+    const size_t n = (size_t)T * k;
+    double* logits = (double*)malloc((size_t)T * E * sizeof(double));
+    double* w = (double*)malloc(n * sizeof(double));
+    int32_t* so = (int32_t*)malloc(n * sizeof(int32_t));
+    int32_t* cnt = (int32_t*)malloc(((size_t)S + 1) * sizeof(int32_t));
+    int32_t* off = (int32_t*)malloc(((size_t)S + 2) * sizeof(int32_t));
+    int32_t* perm = (int32_t*)malloc(n * sizeof(int32_t));
+    int32_t* inv = (int32_t*)malloc(n * sizeof(int32_t));
+    uint8_t* qx = (uint8_t*)malloc((size_t)T * H);
+    float* sx = (float*)malloc((size_t)T * sizeof(float));
+    double* yd = (double*)calloc(n * H, sizeof(double));
+    double* ysh = (double*)calloc((size_t)T * H, sizeof(double));
+    double* tmp = (double*)malloc((size_t)H * sizeof(double));
+
+    oracle_router_logits(s, T, x, w_router, bias, logits);
+    oracle_topk_softmax(T, E, k, logits, idx, w);
+    const int invalid = oracle_slot_map(s, T, idx, replica_of, so);
+    oracle_histogram(s, (int)n, so, cnt, NULL);
+    oracle_dispatch(s, T, so, cnt, NULL, off, perm, inv, NULL);
+    oracle_quantize_rows_e4m3(T, H, x, qx, sx);
+    for (int slot = 0; slot < S; ++slot) {
+        for (int row = off[slot]; row < off[slot + 1]; ++row) {
+            const int t = perm[row] / k;
+            oracle_swiglu_row_fp8(H, I, qx + (size_t)t * H, sx[t], qg + (size_t)slot * I * H, sg + (size_t)slot * I,
+                                  qu + (size_t)slot * I * H, su + (size_t)slot * I, w_down + (size_t)slot * H * I,
+                                  yd + (size_t)row * H);
+        }
+    }
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < s->n_shared; ++j) {
+            oracle_swiglu_row_fp8(H, Is, qx + (size_t)t * H, sx[t], qsg + (size_t)j * Is * H, ssg + (size_t)j * Is,
+                                  qsu + (size_t)j * Is * H, ssu + (size_t)j * Is, ws_down + (size_t)j * H * Is, tmp);
+            for (int o = 0; o < H; ++o) ysh[(size_t)t * H + o] += tmp[o];
+        }
+    }
+    oracle_combine(s, T, yd, inv, w, ysh, out);
+    free(logits); free(w); free(so); free(cnt); free(off); free(perm); free(inv);
+    free(qx); free(sx); free(yd); free(ysh); free(tmp);
+    return invalid;
+}

@@ -141,6 +141,38 @@ void oracle_eplb_window(const oracle_shape* s, int n_batches, const int32_t* his
                         const int32_t* replica_of, double threshold, int64_t* slot_window,
                         int64_t* block_load, int64_t* expert_load, double* ratio, int* trigger);
 
+/* ---- FP8 (section 2.3 of the post: FP8 communication halves the per-token
+ * dispatch + combine bytes, 229 KB -> 115 KB).
+ * E4M3 (OCP 8-bit floating point: 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; largest finite 448; code 0x7F/0xFF is NaN; no infinity).
+ * Encoding rounds to nearest, ties to even, and saturates finite values
+ * beyond 448 to +-448; NaN encodes as 0x7F. */
+uint8_t oracle_e4m3_encode(float v);
+double oracle_e4m3_decode(uint8_t code);
+
+/* Per-row quantisation: scale[r] = amax(|row|) / 448 in fp32 (1 if the row is
+ * all zero); codes[r][c] = e4m3(x[r][c] / scale[r]), the division in fp32.
+ * Dequantised value = decode(code) * scale. */
+void oracle_quantize_rows_e4m3(int rows, int cols, const uint16_t* x_bf16, uint8_t* codes, float* scale);
+
+/* FFN of one row with FP8 gate/up: g_i = sx*sg[i] * sum_c qx_c*qg[i][c] (exact
+ * products of dequantised values in fp64), u likewise, h = silu(g)*u,
+ * y = h W_d^T with the bf16 down weights.  qg/qu [I,H] codes, sg/su [I]. */
+void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
+                           const uint8_t* qu, const float* su, const uint16_t* w_down, double* y);
+
+/* Whole layer with the FP8 dispatch payload and FP8 gate/up weights: routing
+ * as oracle_moe_forward (bf16 router), every token quantised once per row
+ * (its k dispatched copies carry the same codes and scale), routed and shared
+ * gate/up in FP8 (codes qg/qu [S,I,H] with scales [S,I]; shared [n_sh,I_sh,H]
+ * with [n_sh,I_sh]), down projections in bf16, combine as oracle_combine.
+ * Returns the number of invalid expert ids. */
+int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
+                           const float* bias, const int32_t* replica_of, const uint8_t* qg, const float* sg,
+                           const uint8_t* qu, const float* su, const uint16_t* w_down, const uint8_t* qsg,
+                           const float* ssg, const uint8_t* qsu, const float* ssu, const uint16_t* ws_down,
+                           int32_t* idx, double* out);
+
 /* Replica placement for n_rep redundant slots from per-expert counts[E].
  * Hot list: the n_rep experts with the largest counts (ties -> lower id).
  * Each block initially carries the load of its experts, a hot expert's

@@ -457,3 +457,103 @@ def test_eplb_window_matches_histograms_of_recent_batches():
         assert abs(ratio - bl.max() * 4 / bl.sum()) < 1e-15
         _, bl1, _, _, _ = oracle.eplb_window(w, hist[-1:], 1)
         assert np.array_equal(bl1, oracle.histogram(w, oracle.slot_map(w, idx)[0])[1])
+
+
+# ------------------------------------------------------------------ FP8 (E4M3)
+
+
+def test_e4m3_encoder_special_values():
+    vals = [448.0, 500.0, 1e9, 0.0, -0.0, 1.0, -3.5, 2.0 ** -6, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10,
+            1.0625, 1.1875, 0.875, float("nan")]
+    want = [0x7E, 0x7E, 0x7E, 0x00, 0x80, 0x38, 0xC6, 0x08, 0x01, 0x00, 0x02, 0x38, 0x3A, 0x36, 0x7F]
+    assert list(oracle.e4m3_encode(vals)) == want
+    assert oracle.e4m3_decode([0x7E])[0] == 448.0 and oracle.e4m3_decode([0x01])[0] == 2.0 ** -9
+    assert np.isnan(oracle.e4m3_decode([0x7F])[0])
+
+
+def test_e4m3_round_trip_and_monotone():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+    xs = np.sort(np.random.default_rng(0).uniform(-460, 460, 3000)).astype(np.float32)
+    dec = oracle.e4m3_decode(oracle.e4m3_encode(xs))
+    assert np.all(np.diff(dec) >= 0)
+
+
+def test_e4m3_encoder_matches_torch_conversion():
+    rng = np.random.default_rng(1)
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    grid = np.sort(np.abs(oracle.e4m3_decode(codes)))
+    mids = (grid[1:] + grid[:-1]) / 2  # exact ties between neighbours
+    xs = np.concatenate([rng.uniform(-448, 448, 4000), rng.normal(0, 0.01, 2000), mids, -mids,
+                         np.nextafter(mids, 0), np.nextafter(mids, 1000)]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(xs), ref)
+
+
+def test_row_quantizer_scale_and_error_bound():
+    x = _bf16((12, 96), 2.0, 3, 1)
+    x[5] = 0
+    codes, scale = oracle.quantize_rows_e4m3(x)
+    xf = x.float().numpy().astype(np.float64)
+    amax = np.abs(xf).max(axis=1)
+    assert scale[5] == 1.0 and np.all(codes[5] == 0)
+    np.testing.assert_array_equal(scale[amax > 0], (amax[amax > 0].astype(np.float32) / np.float32(448.0)))
+    deq = oracle.e4m3_decode(codes).reshape(codes.shape) * scale[:, None].astype(np.float64)
+    normal = np.abs(xf) >= 2.0 ** -6 * scale[:, None]
+    err = np.abs(deq - xf)
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(xf[normal]) * 1.0000001)  # half an ulp of 3 mantissa bits
+    assert np.all(err[~normal] <= 2.0 ** -10 * scale[:, None].repeat(96, 1)[~normal] * 1.0000001)
+
+
+def test_fp8_swiglu_row_reduces_to_bf16_on_exact_values():
+    rng = np.random.default_rng(4)
+    H, I = 48, 24
+    grid = np.array([0.0, 0.25, 0.5, 0.75, 1.0, 1.5, 2.0, -0.25, -0.5, -1.0, -1.5, -2.0])
+    xv, gv, uv = rng.choice(grid, H), rng.choice(grid, (I, H)) / 4, rng.choice(grid, (I, H)) / 4
+    d = _bf16((H, I), I ** -0.5, 5, 5)
+    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    y8 = oracle.swiglu_row_fp8(oracle.e4m3_encode(xv), 1.0, oracle.e4m3_encode(gv).reshape(I, H), np.ones(I),
+                               oracle.e4m3_encode(uv).reshape(I, H), np.ones(I), d)
+    y = oracle.swiglu_row(to_bf16(xv), to_bf16(gv), to_bf16(uv), d)
+    np.testing.assert_allclose(y8, y, rtol=1e-13, atol=1e-15)
+    # scales factor out of the sums
+    y8s = oracle.swiglu_row_fp8(oracle.e4m3_encode(xv), 2.0, oracle.e4m3_encode(gv).reshape(I, H), np.full(I, 0.5),
+                                oracle.e4m3_encode(uv).reshape(I, H), np.full(I, 0.25), d)
+    y2 = oracle.swiglu_row(to_bf16(xv), to_bf16(gv), to_bf16(uv / 2), d)
+    np.testing.assert_allclose(y8s, y2, rtol=1e-13, atol=1e-15)
+
+
+def _fp8_weights(w, wg, wu, wd, sg_, su_, sd_):
+    qg, sgs = oracle.quantize_rows_e4m3(wg.reshape(-1, w.hidden))
+    qu, sus = oracle.quantize_rows_e4m3(wu.reshape(-1, w.hidden))
+    qsg, ssg = oracle.quantize_rows_e4m3(sg_.reshape(-1, w.hidden))
+    qsu, ssu = oracle.quantize_rows_e4m3(su_.reshape(-1, w.hidden))
+    return dict(qg=qg, sg=sgs, qu=qu, su=sus, wd=wd, qsg=qsg, ssg=ssg, qsu=qsu, ssu=ssu)
+
+
+def test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors():
+    w = _tiny(top_k=3, n_shared=2, inter_shared=24, tokens=21)
+    x, wr, _, wg, wu, wd, sg, su, sd = _tiny_inputs(w)
+    q = _fp8_weights(w, wg, wu, wd, sg, su, sd)
+    r = oracle.moe_forward_fp8(w, x, wr, None, None, q, sd)
+    deq = lambda c, s_: torch.from_numpy(oracle.e4m3_decode(c).reshape(c.shape) * s_[:, None].astype(np.float64))
+    qx, sx = oracle.quantize_rows_e4m3(x)
+    xq = deq(qx, sx)
+    G = deq(q["qg"], q["sg"]).reshape(w.n_experts, w.inter, w.hidden)
+    U = deq(q["qu"], q["su"]).reshape(w.n_experts, w.inter, w.hidden)
+    SG = deq(q["qsg"], q["ssg"]).reshape(w.n_shared, w.inter_shared, w.hidden)
+    SU = deq(q["qsu"], q["ssu"]).reshape(w.n_shared, w.inter_shared, w.hidden)
+    logits = _f64(x) @ _f64(wr).T
+    p = torch.softmax(logits, -1)
+    top = torch.topk(logits, w.top_k, -1).indices
+    ref = torch.zeros(w.tokens, w.hidden, dtype=torch.float64)
+    for e in range(w.n_experts):
+        y = F.linear(F.silu(F.linear(xq, G[e])) * F.linear(xq, U[e]), _f64(wd[e]))
+        ref += ((top == e).any(-1).double() * p[:, e])[:, None] * y
+    for j in range(w.n_shared):
+        ref += F.linear(F.silu(F.linear(xq, SG[j])) * F.linear(xq, SU[j]), _f64(sd[j]))
+    assert np.array_equal(np.sort(r["idx"], 1), np.sort(top.numpy(), 1))
+    np.testing.assert_allclose(r["out"], ref.numpy(), rtol=1e-11, atol=1e-12 * ref.abs().max().item())
+    # and it stays close to the bf16 layer
+    r16 = oracle.moe_forward(w, x, wr, None, None, wg, wu, wd, sg, su, sd)
+    assert np.linalg.norm(r["out"] - r16["out"]) / np.linalg.norm(r16["out"]) < 0.1

@@ -39,6 +39,13 @@ MUTANTS = [
      "(void)replica_of;"),
     ("trigger compares the mean", "*trigger = (double)mx * (double)B > threshold * (double)total;",
      "*trigger = (double)total > threshold * (double)total;"),
+    ("e4m3 ties round away from zero", "const double m = rint(a * ldexp(1.0, 9));",
+     "const double m = round(a * ldexp(1.0, 9));"),
+    ("e4m3 normal mantissa truncated", "double m = rint((a * ldexp(1.0, -e) - 1.0) * 8.0);",
+     "double m = floor((a * ldexp(1.0, -e) - 1.0) * 8.0);"),
+    ("row scale uses the wrong maximum", "const float s = amax > 0.0f ? amax / 448.0f : 1.0f;",
+     "const float s = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    ("fp8 gate ignores the token scale", "g *= (double)sx * (double)sg[i];", "g *= (double)sg[i];"),
     ("home slot ignores the replica slots", "return (e / epb) * spb + (e % epb);", "return e;"),
     ("replica used by even tokens", "replica_of[e] >= 0 && (t % 2) == 1", "replica_of[e] >= 0 && (t % 2) == 0"),
     ("dispatch fills slots in reverse order", "for (int a = 0; a < n; ++a) {\n        const int32_t slot = slot_of[a];",
@@ -79,6 +86,12 @@ PINS = [
     pins.test_replica_plan_hot_list_ties_go_to_lower_id,
     pins.test_replica_plan_falls_back_to_home_block,
     pins.test_replicated_layer_equals_plain_layer_exactly,
+    pins.test_e4m3_encoder_special_values,
+    pins.test_e4m3_round_trip_and_monotone,
+    pins.test_e4m3_encoder_matches_torch_conversion,
+    pins.test_row_quantizer_scale_and_error_bound,
+    pins.test_fp8_swiglu_row_reduces_to_bf16_on_exact_values,
+    pins.test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors,
     pins.test_eplb_window_hand_case,
     pins.test_eplb_window_matches_histograms_of_recent_batches,
 ]
