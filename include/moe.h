@@ -285,6 +285,46 @@ MOE_API int moe_expert_ffn_noalloc(const moe_shape_t* shape, int T, const void* 
                                    const void* w_down, const void* ws_gate, const void* ws_up,
                                    const void* ws_down, void* y_disp, float* y_shared, int mode, void* stream);
 
+/* ---------------------------------------------------------------- FP8 path
+ * Section 2.3: FP8 communication halves the per-token dispatch + combine
+ * volume.  Format E4M3 (OCP 8-bit float: 4 exponent bits, bias 7, 3 mantissa
+ * bits, largest finite 448).  A row is stored as codes plus one fp32 scale:
+ * scale = amax(|row|) / 448 (1 for an all-zero row), code = e4m3(x / scale)
+ * rounded to nearest even with saturation (the division in fp32); its value
+ * is decode(code) * scale.
+ *
+ * moe_quantize_rows_fp8: rows x cols bf16 -> codes [rows, cols] u8 and
+ * scale [rows] fp32 (cols % 16 == 0).  Use it once on the expert gate and up
+ * weights ([S*I, H] and [n_sh*I_sh, H]: one scale per output row).
+ * moe_dispatch_fp8: moe_dispatch, except that each token is quantised once
+ * (x8 [T,H] u8, x_scale [T]) and its dispatched copies carry its codes and
+ * scale (x_disp8 [T*k,H] u8, x_disp_scale [T*k]): the dispatch buffer is
+ * T*k*H bytes, half of the bf16 one (57,344 B per token at k=8, H=7168).
+ * moe_expert_gate_up_fp8: moe_expert_gate_up with E4M3 operands on the FP8
+ * tensor cores; h = silu(g) * u with g = sx*sg[i]*sum(qx*qg) (fp32 accumulate),
+ * u likewise; h out in bf16, as for moe_expert_gate_up.  The down projection
+ * stays bf16 (moe_expert_down).  hidden % 16 == 0.
+ * moe_forward_fp8: route (bf16 router), moe_dispatch_fp8,
+ * moe_expert_gate_up_fp8, moe_expert_down, moe_combine, intermediates in a
+ * workspace of moe_workspace_size_fp8() bytes. */
+MOE_API int moe_quantize_rows_fp8(int rows, int cols, const void* x, uint8_t* codes, float* scale, void* stream);
+MOE_API int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
+                             const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
+                             int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint8_t* x8, float* x_scale,
+                             uint8_t* x_disp8, float* x_disp_scale, void* stream);
+MOE_API int moe_expert_gate_up_fp8(const moe_shape_t* shape, int T, const uint8_t* x8, const float* x_scale,
+                                   const uint8_t* x_disp8, const float* x_disp_scale, const int32_t* offsets,
+                                   const uint8_t* qg, const float* sg, const uint8_t* qu, const float* su,
+                                   const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
+                                   void* h_disp, void* h_shared, int mode, void* stream);
+MOE_API size_t moe_workspace_size_fp8(const moe_shape_t* shape, int T);
+MOE_API int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
+                            const int32_t* replica_of, const uint8_t* qg, const float* sg, const uint8_t* qu,
+                            const float* su, const void* w_down, const uint8_t* qsg, const float* ssg,
+                            const uint8_t* qsu, const float* ssu, const void* ws_down, void* out,
+                            int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out, int32_t* block_counts_out,
+                            int mode, void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- steps 4-5: combine
  * Section 2.2 steps 4-5 (shared expert gate taken as 1):
  *   out[t,:] = bf16( sum_{j<k} topk_w[t,j] * y_disp[inv_perm[t*k+j], :] + y_shared[t,:] ),

@@ -37,7 +37,8 @@ EXPORTS = (
     "moe_expert_down", "moe_ffn_workspace_size", "moe_expert_ffn", "moe_combine",
     "moe_workspace_size", "moe_forward", "moe_expert_ffn_noalloc", "moe_route_grouped",
     "moe_eplb_window_bytes", "moe_eplb_window_reset", "moe_eplb_window_push", "moe_eplb_stable_table",
-    "moe_eplb_copy_replicas",
+    "moe_eplb_copy_replicas", "moe_quantize_rows_fp8", "moe_dispatch_fp8", "moe_expert_gate_up_fp8",
+    "moe_workspace_size_fp8", "moe_forward_fp8",
 )
 
 # capacity of the fixed scratch of moe_expert_ffn_noalloc (include/moe.h)
@@ -89,6 +90,11 @@ _SIG = {
     "moe_expert_ffn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
     "moe_expert_ffn_noalloc": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_quantize_rows_fp8": (_I, [_I, _I, _P, _P, _P, _P]),
+    "moe_dispatch_fp8": (_I, [_P, _I] + [_P] * 13 + [_P]),
+    "moe_expert_gate_up_fp8": (_I, [_P, _I] + [_P] * 15 + [_I, _P]),
+    "moe_workspace_size_fp8": (_Z, [_P, _I]),
+    "moe_forward_fp8": (_I, [_P, _I] + [_P] * 19 + [_I, _P, _Z, _P]),
     "moe_workspace_size": (_Z, [_P, _I]),
     "moe_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
 }
@@ -292,3 +298,41 @@ def moe_forward(shape, T, x, w_router, bias, replica_of, w_gate, w_up, w_down, w
                              _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down),
                              _ptr(out), _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out),
                              _ptr(block_counts_out), mode, _ptr(ws), ws_bytes, _stream(stream)))
+
+
+# ------------------------------------------------------------------ FP8 path
+
+def moe_quantize_rows_fp8(x, codes, scale, stream=None):
+    rows = x.shape[0]
+    cols = x.numel() // max(1, rows)
+    _check(lib().moe_quantize_rows_fp8(rows, cols, _ptr(x), _ptr(codes), _ptr(scale), _stream(stream)))
+
+
+def moe_dispatch_fp8(shape, T, x, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm,
+                     x8, x_scale, x_disp8, x_disp_scale, stream=None):
+    _check(lib().moe_dispatch_fp8(_shape(shape), T, _ptr(x), _ptr(topk_idx), _ptr(replica_of), _ptr(slot_of),
+                                  _ptr(counts), _ptr(block_counts), _ptr(offsets), _ptr(perm), _ptr(inv_perm),
+                                  _ptr(x8), _ptr(x_scale), _ptr(x_disp8), _ptr(x_disp_scale), _stream(stream)))
+
+
+def moe_expert_gate_up_fp8(shape, T, x8, x_scale, x_disp8, x_disp_scale, offsets, qg, sg, qu, su, qsg, ssg, qsu,
+                           ssu, h_disp, h_shared, mode=MOE_FFN_AUTO, stream=None):
+    _check(lib().moe_expert_gate_up_fp8(_shape(shape), T, _ptr(x8), _ptr(x_scale), _ptr(x_disp8),
+                                        _ptr(x_disp_scale), _ptr(offsets), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su),
+                                        _ptr(qsg), _ptr(ssg), _ptr(qsu), _ptr(ssu), _ptr(h_disp), _ptr(h_shared),
+                                        mode, _stream(stream)))
+
+
+def moe_workspace_size_fp8(shape, T: int) -> int:
+    return lib().moe_workspace_size_fp8(_shape(shape), T)
+
+
+def moe_forward_fp8(shape, T, x, w_router, bias, replica_of, qg, sg, qu, su, w_down, qsg, ssg, qsu, ssu, ws_down,
+                    out, topk_idx_out=None, topk_w_out=None, counts_out=None, block_counts_out=None,
+                    mode=MOE_FFN_AUTO, ws=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(lib().moe_forward_fp8(_shape(shape), T, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(replica_of),
+                                 _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(w_down), _ptr(qsg), _ptr(ssg),
+                                 _ptr(qsu), _ptr(ssu), _ptr(ws_down), _ptr(out), _ptr(topk_idx_out),
+                                 _ptr(topk_w_out), _ptr(counts_out), _ptr(block_counts_out), mode, _ptr(ws),
+                                 ws_bytes, _stream(stream)))

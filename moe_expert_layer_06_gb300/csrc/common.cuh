@@ -153,6 +153,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A * B^T with E4M3 inputs (kind::f8f6f4, K = 32 per instruction), fp32 accumulate.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -194,6 +205,13 @@ __host__ __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
     return (1u << 4)                          // D = f32
            | (1u << 7)                        // A = bf16
            | (1u << 10)                       // B = bf16
+           | ((uint32_t)(N >> 3) << 17)       // N / 8
+           | ((uint32_t)(M >> 4) << 24);      // M / 16
+}
+
+// Instruction descriptor, kind::f8f6f4: E4M3 A and B (format code 0, both K-major), fp32 D.
+__host__ __device__ __forceinline__ uint32_t umma_idesc_e4m3(int M, int N) {
+    return (1u << 4)                          // D = f32
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }

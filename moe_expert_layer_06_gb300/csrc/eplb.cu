@@ -26,7 +26,6 @@ struct WindowHeader {
 };
 
 // State layout: header | ring [window][S+1] int32 | sums [S+1] int64 (8-byte aligned).
-inline size_t ring_offset() { return sizeof(WindowHeader); }
 __host__ __device__ inline size_t sum_offset(int window, int S) {
     const size_t ring_end = sizeof(WindowHeader) + (size_t)window * (S + 1) * sizeof(int32_t);
     return (ring_end + 15) & ~size_t(15);

@@ -49,6 +49,9 @@ template <int MODE>
 struct Traits {
     static constexpr int NA = (MODE == kRouter) ? 1 : 2;
     static constexpr int kRowsPerItem = (MODE == kDown) ? 256 : 128;
+    static constexpr bool kGateUpLike = (MODE == kGateUp || MODE == kGateUpF8);
+    // elements of K per 128-byte smem row (one pipeline chunk)
+    static constexpr int kChunkK = (MODE == kGateUpF8) ? 128 : 64;
 };
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
@@ -104,7 +107,7 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Tabl
         const int mb = cdiv(a.m_shared, RPI);
         it.shared = 1;
         int r = i;
-        if (MODE == kGateUp) {
+        if (Traits<MODE>::kGateUpLike) {
             it.z = r / (mb * chunks);
             r -= it.z * mb * chunks;
         } else {
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (MODE != kRouter && a.n_shared > 0) {
         const int chunks = cdiv(a.T, BN);
         const int mb = cdiv(a.m_shared, RPI);
-        n_sh_items = (MODE == kGateUp ? a.n_shared : 1) * mb * chunks;
+        n_sh_items = (Traits<MODE>::kGateUpLike ? a.n_shared : 1) * mb * chunks;
     }
     int n_items;
     if (MODE == kRouter) {
@@ -258,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     armed[stage] = phase;
-                    int ka = kc * 64, kb = kc * 64, za = it.z, bmid = 0;
+                    constexpr int CK = Traits<MODE>::kChunkK;
+                    int ka = kc * CK, kb = kc * CK, za = it.z, bmid = 0;
                     if (MODE == kDown && it.shared) {
                         za = kc / a.kc_per_sh;
                         ka = (kc - za * a.kc_per_sh) * 64;
@@ -266,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         bmid = za;
                     }
                     tma_load_3d(smem_u32(sa), ma0, fb, ka, it.m0, za, pol_w);
-                    if (MODE == kGateUp) tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
+                    if (Traits<MODE>::kGateUpLike)
+                        tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
                     if (MODE == kDown) tma_load_3d(smem_u32(sa + kABytes), ma0, fb, ka, it.m0 + 128, za, pol_w);
                     for (int bit = 3, off = 0; bit >= 0; --bit) {
                         if (nb & (1 << bit)) {
@@ -297,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
                 const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
                 const int nb = (it.nrows + 15) >> 4;
-                const uint32_t idesc = umma_idesc_bf16(128, nb * 16);
+                const uint32_t idesc =
+                    MODE == kGateUpF8 ? umma_idesc_e4m3(128, nb * 16) : umma_idesc_bf16(128, nb * 16);
                 if (*abort_flag || !mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, limit)) {
                     ok = false;
                     break;
@@ -317,8 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (kc > it.kc0 || kk > 0) ? 1u : 0u;
-                        umma_bf16(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, accum);
-                        if (NA == 2) umma_bf16(d0 + BN, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                        // 32 bytes of K per instruction: 16 bf16 or 32 e4m3 elements
+                        if (MODE == kGateUpF8) {
+                            umma_e4m3(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                            umma_e4m3(d0 + BN, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                        } else {
+                            umma_bf16(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                            if (NA == 2) umma_bf16(d0 + BN, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                        }
                     }
                     umma_commit(smem_u32(&empty[stage]));
                     if (++stage == STAGES) {
@@ -367,8 +379,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 tmem_ld16(tl + g * 16, v0);
                 if (NA == 2) tmem_ld16(tl + BN + g * 16, v1);
                 tmem_ld_wait();
-                if (MODE == kGateUp) {
+                if (Traits<MODE>::kGateUpLike) {
                     if (row_ok) {
+                        if (MODE == kGateUpF8) {
+                            // dequantise: weight-row scale x token scale (both factor out of the K sum)
+                            const float* sa0 = it.shared ? a.sa0_scale + (size_t)it.z * a.m_shared
+                                                         : a.a0_scale + (size_t)it.z * a.m_routed;
+                            const float* sa1 = it.shared ? a.sa1_scale + (size_t)it.z * a.m_shared
+                                                         : a.a1_scale + (size_t)it.z * a.m_routed;
+                            const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
+                            const float wg = __ldg(sa0 + mrow), wu = __ldg(sa1 + mrow);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int col = g * 16 + j;
+                                const float sx = col < it.nrows ? __ldg(sbp + col) : 0.0f;
+                                v0[j] *= wg * sx;
+                                v1[j] *= wu * sx;
+                            }
+                        }
                         __nv_bfloat16* dst;
                         int ld;
                         if (it.shared) {
@@ -462,12 +490,14 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, c
     if (grid <= 0) return cudaSuccess;
     if (bn == 32) {
         switch (mode) {
+            case kGateUpF8: return launch_one<kGateUpF8, 32, 5>(args, grid, stream);
             case kGateUp: return launch_one<kGateUp, 32, 5>(args, grid, stream);
             case kDown: return launch_one<kDown, 32, 5>(args, grid, stream);
             case kRouter: return launch_one<kRouter, 32, 8>(args, grid, stream);
         }
     } else if (bn == kPrefillBN) {
         switch (mode) {
+            case kGateUpF8: return launch_one<kGateUpF8, kPrefillBN, 4>(args, grid, stream);
             case kGateUp: return launch_one<kGateUp, kPrefillBN, 4>(args, grid, stream);
             case kDown: return launch_one<kDown, kPrefillBN, 4>(args, grid, stream);
             case kRouter: return launch_one<kRouter, kPrefillBN, 5>(args, grid, stream);

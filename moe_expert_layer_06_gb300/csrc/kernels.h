@@ -13,7 +13,10 @@
 namespace moe {
 
 // ---------------------------------------------------------------- grouped swap-AB GEMM (tcgen05)
-enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2 };
+// kGateUpF8: gate/up with E4M3 weights and tokens (128-element K chunks,
+// tcgen05 kind::f8f6f4), per-row weight scales and per-token scales applied
+// in the epilogue (they factor out of the K sum).
+enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2, kGateUpF8 = 3 };
 
 // One launch computes D = A * B^T for a list of work items.  A is a weight
 // tile of 128 output rows (the UMMA M operand), B is a chunk of up to BN
@@ -44,6 +47,13 @@ struct GemmArgs {
     void* out_sh;     // h_sh bf16 [T, n_sh*I_sh] | y_sh f32 [T,H]
     int out_sh_ld;
     int sh_col_stride;  // gate/up: I_sh (column offset of shared expert j in h_sh)
+    // FP8 gate/up only: dequantisation scales
+    const float* a0_scale;  // routed gate rows [S*I]
+    const float* a1_scale;  // routed up rows [S*I]
+    const float* sa0_scale; // shared gate rows [n_sh*I_sh]
+    const float* sa1_scale; // shared up rows [n_sh*I_sh]
+    const float* b_scale;   // dispatched token rows [T*k]
+    const float* sb_scale;  // tokens [T]
     DevStatus st;
 };
 
@@ -60,7 +70,16 @@ int gemm_max_slots();
 // 3-D bf16 tensor map, dims innermost first (elements), strides of dims 1,2 in bytes.
 int make_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
-                 uint32_t box2);
+                 uint32_t box2, bool fp8 = false);
+
+// ---------------------------------------------------------------- FP8 (E4M3) quantisation
+// codes[r][c] = e4m3(x[r][c] / scale[r]), scale[r] = amax(|x[r]|) / 448 (1 for a zero row),
+// round to nearest even with saturation; cols % 8 == 0.
+cudaError_t launch_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t* codes, float* scale,
+                                 cudaStream_t stream);
+// x_disp8[row] = x8[perm[row] / k] (row_bytes per row, 16-byte vectors), x_disp_scale[row] likewise.
+cudaError_t launch_scatter_fp8(const uint8_t* x8, const float* x_scale, const int32_t* perm, int n_rows, int k,
+                               int row_bytes, uint8_t* x_disp8, float* x_disp_scale, cudaStream_t stream);
 
 // ---------------------------------------------------------------- routing
 // Top-k over the (K-split) router logits; n_groups > topk_groups restricts the

@@ -92,14 +92,15 @@ static EncodeTiledFn encode_fn() {
 }
 
 int make_tmap_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
-                 uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2) {
+                 uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2, bool fp8) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {stride1, stride2};
     const cuuint32_t box[3] = {box0, box1, box2};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -127,6 +128,21 @@ static int tmap_hsh(CUtensorMap* m, const void* p, int T, int n_sh, int I_sh) {
     for (int j = 0; j < 4; ++j) {
         const int rc = make_tmap_3d(m + j, p, (uint64_t)I_sh, (uint64_t)n_sh, (uint64_t)T, (uint64_t)I_sh * 2,
                                     (uint64_t)I_sh * n_sh * 2, 64, 1, 16u << j);
+        if (rc) return rc;
+    }
+    return MOE_OK;
+}
+
+// FP8 (one byte per element, 128-element rows per chunk)
+static int tmap_weights_f8(CUtensorMap* m, const void* p, int n, int rows, int K) {
+    return make_tmap_3d(m, p, (uint64_t)K, (uint64_t)rows, (uint64_t)n, (uint64_t)K, (uint64_t)K * rows, 128, 128, 1,
+                        true);
+}
+
+static int tmap_rows_f8(CUtensorMap* m, const void* p, int rows, int K) {
+    for (int j = 0; j < 4; ++j) {
+        const int rc = make_tmap_3d(m + j, p, (uint64_t)K, 1, (uint64_t)rows, (uint64_t)K, (uint64_t)K, 128, 1,
+                                    16u << j, true);
         if (rc) return rc;
     }
     return MOE_OK;
@@ -330,6 +346,73 @@ static int gate_up_impl(const moe_shape_t* s, int T, const void* x, const void* 
     return MOE_OK;
 }
 
+static int gate_up_fp8_impl(const moe_shape_t* s, int T, const void* x8, const float* x_scale, const void* x_disp8,
+                            const float* x_disp_scale, const int32_t* offsets, const void* qg, const float* sg,
+                            const void* qu, const float* su, const void* qsg, const float* ssg, const void* qsu,
+                            const float* ssu, void* h_disp, void* h_shared, int mode, cudaStream_t stream) {
+    if (s->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
+    NEED(x_disp8, "x_disp8");
+    NEED4(x_disp_scale, "x_disp_scale");
+    NEED4(offsets, "offsets");
+    NEED(qg, "qg");
+    NEED(qu, "qu");
+    NEED4(sg, "sg");
+    NEED4(su, "su");
+    NEED(h_disp, "h_disp");
+    const int n_sh = s->n_shared;
+    if (n_sh > 0) {
+        NEED(x8, "x8");
+        NEED4(x_scale, "x_scale");
+        NEED(qsg, "qsg");
+        NEED(qsu, "qsu");
+        NEED4(ssg, "ssg");
+        NEED4(ssu, "ssu");
+        NEED(h_shared, "h_shared");
+    }
+    DevStatus st;
+    int rc = device_status(&st);
+    if (rc) return rc;
+    const int n = T * s->top_k;
+    const int bn = ffn_bn(T, mode);
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    if ((rc = tmap_weights_f8(&g.a0, qg, s->n_slots, s->inter, s->hidden))) return rc;
+    if ((rc = tmap_weights_f8(&g.a1, qu, s->n_slots, s->inter, s->hidden))) return rc;
+    if ((rc = tmap_rows_f8(g.b, x_disp8, n, s->hidden))) return rc;
+    if (n_sh > 0) {
+        if ((rc = tmap_weights_f8(&g.sa0, qsg, n_sh, s->inter_shared, s->hidden))) return rc;
+        if ((rc = tmap_weights_f8(&g.sa1, qsu, n_sh, s->inter_shared, s->hidden))) return rc;
+        if ((rc = tmap_rows_f8(g.sb, x8, T, s->hidden))) return rc;
+    } else {
+        g.sa0 = g.a0;
+        g.sa1 = g.a1;
+        for (int j = 0; j < 4; ++j) g.sb[j] = g.b[j];
+    }
+    g.offsets = offsets;
+    g.n_slots = s->n_slots;
+    g.T = T;
+    g.m_routed = s->inter;
+    g.kc_routed = (s->hidden + 127) / 128;
+    g.n_shared = n_sh;
+    g.m_shared = s->inter_shared;
+    g.kc_shared = (s->hidden + 127) / 128;
+    g.kc_per_sh = 1;
+    g.out = h_disp;
+    g.out_ld = s->inter;
+    g.out_sh = h_shared;
+    g.out_sh_ld = n_sh * s->inter_shared;
+    g.sh_col_stride = s->inter_shared;
+    g.a0_scale = sg;
+    g.a1_scale = su;
+    g.sa0_scale = ssg;
+    g.sa1_scale = ssu;
+    g.b_scale = x_disp_scale;
+    g.sb_scale = x_scale;
+    g.st = st;
+    MOE_CUDA(launch_gemm(kGateUpF8, bn, g, num_sms(), stream), "FP8 gate/up gemm launch");
+    return MOE_OK;
+}
+
 static int down_impl(const moe_shape_t* s, int T, const void* h_disp, const void* h_shared, const int32_t* offsets,
                      const void* w_down, const void* ws_down, void* y_disp, float* y_shared, int mode,
                      cudaStream_t stream) {
@@ -411,6 +494,30 @@ static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
     L.ffn = take(ffn_ws(s, T));
     L.y_disp = take(n * s->hidden * 2);
     L.y_sh = take((size_t)T * s->hidden * 4);
+    L.total = off;
+    return L;
+}
+
+// FP8 forward: the bf16 layout plus the quantised tokens and their dispatched copies
+struct FwdLayoutF8 {
+    FwdLayout base;
+    size_t x8, x_scale, x_disp8, x_disp_scale, total;
+};
+
+static FwdLayoutF8 fwd_layout_f8(const moe_shape_t* s, int T) {
+    FwdLayoutF8 L;
+    L.base = fwd_layout(s, T);
+    const size_t n = (size_t)T * s->top_k;
+    size_t off = L.base.total;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    L.x8 = take((size_t)T * s->hidden);
+    L.x_scale = take((size_t)T * 4);
+    L.x_disp8 = take(n * s->hidden);
+    L.x_disp_scale = take(n * 4);
     L.total = off;
     return L;
 }
@@ -712,6 +819,110 @@ int moe_forward(const moe_shape_t* shape, int T, const void* x, const void* w_ro
                              b + L.y_disp, y_sh, mode, b + L.ffn, ffn_ws(shape, T), stream)))
         return rc;
     return moe_combine(shape, T, b + L.y_disp, inv, tw, y_sh, out, stream);
+}
+
+int moe_quantize_rows_fp8(int rows, int cols, const void* x, uint8_t* codes, float* scale, void* stream) {
+    if (rows < 0 || cols <= 0 || cols % 16) return fail(MOE_ERR_INVALID_ARG, "rows >= 0 and cols %% 16 == 0 required");
+    if (rows == 0) return MOE_OK;
+    NEED(x, "x");
+    NEED(codes, "codes");
+    NEED4(scale, "scale");
+    MOE_CUDA(launch_quantize_rows(static_cast<const uint16_t*>(x), rows, cols, codes, scale, as_stream(stream)),
+             "quantize launch");
+    return MOE_OK;
+}
+
+int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
+                     const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
+                     int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint8_t* x8, float* x_scale,
+                     uint8_t* x_disp8, float* x_disp_scale, void* stream) {
+    int rc = check_shape(shape, T);
+    if (rc) return rc;
+    if (shape->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
+    NEED4(counts, "counts");
+    NEED4(offsets, "offsets");
+    if (T == 0) return moe_dispatch(shape, 0, x, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm,
+                                    inv_perm, nullptr, stream);
+    NEED(x, "x");
+    NEED4(topk_idx, "topk_idx");
+    NEED4(slot_of, "slot_of");
+    NEED4(perm, "perm");
+    NEED4(inv_perm, "inv_perm");
+    NEED(x8, "x8");
+    NEED4(x_scale, "x_scale");
+    NEED(x_disp8, "x_disp8");
+    NEED4(x_disp_scale, "x_disp_scale");
+    if (replica_of) NEED4(replica_of, "replica_of");
+    cudaStream_t st = as_stream(stream);
+    if ((rc = index_impl(shape, T, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm, st)))
+        return rc;
+    MOE_CUDA(launch_quantize_rows(static_cast<const uint16_t*>(x), T, shape->hidden, x8, x_scale, st),
+             "quantize launch");
+    MOE_CUDA(launch_scatter_fp8(x8, x_scale, perm, T * shape->top_k, shape->top_k, shape->hidden, x_disp8,
+                                x_disp_scale, st),
+             "FP8 scatter launch");
+    return MOE_OK;
+}
+
+int moe_expert_gate_up_fp8(const moe_shape_t* shape, int T, const uint8_t* x8, const float* x_scale,
+                           const uint8_t* x_disp8, const float* x_disp_scale, const int32_t* offsets,
+                           const uint8_t* qg, const float* sg, const uint8_t* qu, const float* su,
+                           const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
+                           void* h_disp, void* h_shared, int mode, void* stream) {
+    int rc = check_shape(shape, T);
+    if (rc) return rc;
+    if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
+    if (T == 0) return MOE_OK;
+    return gate_up_fp8_impl(shape, T, x8, x_scale, x_disp8, x_disp_scale, offsets, qg, sg, qu, su, qsg, ssg, qsu,
+                            ssu, h_disp, h_shared, mode, as_stream(stream));
+}
+
+size_t moe_workspace_size_fp8(const moe_shape_t* shape, int T) {
+    if (check_shape(shape, T)) return 0;
+    return fwd_layout_f8(shape, T).total;
+}
+
+int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
+                    const int32_t* replica_of, const uint8_t* qg, const float* sg, const uint8_t* qu,
+                    const float* su, const void* w_down, const uint8_t* qsg, const float* ssg, const uint8_t* qsu,
+                    const float* ssu, const void* ws_down, void* out, int32_t* topk_idx_out, float* topk_w_out,
+                    int32_t* counts_out, int32_t* block_counts_out, int mode, void* ws, size_t ws_bytes,
+                    void* stream) {
+    int rc = check_shape(shape, T);
+    if (rc) return rc;
+    if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
+    if (shape->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
+    if (T == 0) return MOE_OK;
+    NEED(out, "out");
+    const FwdLayoutF8 L = fwd_layout_f8(shape, T);
+    if (!ws || ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, L.total);
+    if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    const FwdLayout& B = L.base;
+    int32_t* idx = topk_idx_out ? topk_idx_out : reinterpret_cast<int32_t*>(b + B.idx);
+    float* tw = topk_w_out ? topk_w_out : reinterpret_cast<float*>(b + B.w);
+    int32_t* counts = counts_out ? counts_out : reinterpret_cast<int32_t*>(b + B.counts);
+    int32_t* blocks = block_counts_out ? block_counts_out : reinterpret_cast<int32_t*>(b + B.blocks);
+    int32_t* offsets = reinterpret_cast<int32_t*>(b + B.offsets);
+    int32_t* perm = reinterpret_cast<int32_t*>(b + B.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(b + B.inv_perm);
+    float* y_sh = shape->n_shared > 0 ? reinterpret_cast<float*>(b + B.y_sh) : nullptr;
+    uint8_t* h = b + B.ffn;
+    uint8_t* hs = shape->n_shared > 0 ? h + align256((size_t)T * shape->top_k * shape->inter * 2) : nullptr;
+    if ((rc = moe_route(shape, T, x, w_router, bias, nullptr, nullptr, idx, tw, b + B.route, route_ws(shape, T),
+                        stream)))
+        return rc;
+    if ((rc = moe_dispatch_fp8(shape, T, x, idx, replica_of, reinterpret_cast<int32_t*>(b + B.slot_of), counts,
+                               blocks, offsets, perm, inv, b + L.x8, reinterpret_cast<float*>(b + L.x_scale),
+                               b + L.x_disp8, reinterpret_cast<float*>(b + L.x_disp_scale), stream)))
+        return rc;
+    if ((rc = moe_expert_gate_up_fp8(shape, T, b + L.x8, reinterpret_cast<float*>(b + L.x_scale), b + L.x_disp8,
+                                     reinterpret_cast<float*>(b + L.x_disp_scale), offsets, qg, sg, qu, su, qsg, ssg,
+                                     qsu, ssu, h, hs, mode, stream)))
+        return rc;
+    if ((rc = moe_expert_down(shape, T, h, hs, offsets, w_down, ws_down, b + B.y_disp, y_sh, mode, stream)))
+        return rc;
+    return moe_combine(shape, T, b + B.y_disp, inv, tw, y_sh, out, stream);
 }
 
 }  // extern "C"
