@@ -127,17 +127,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def layer_bytes_flops(w, counts_np):
-    """Algorithmic bytes and flops of one layer pass (touched expert weights read once)."""
+def layer_bytes_flops(w, counts_np, fp8=False):
+    """Algorithmic bytes and flops of one layer pass (touched expert weights read once).
+
+    fp8: gate/up weights and the dispatch payload are one byte per element.
+    """
     H, I, E, k, T = w.hidden, w.inter, w.n_experts, w.top_k, w.tokens
+    gb = 1 if fp8 else 2  # bytes per gate/up weight and per dispatched element
     touched = int((counts_np[:w.n_slots] > 0).sum())
-    expert_bytes = 3 * H * I * 2
-    shared_bytes = w.n_shared * 3 * H * w.inter_shared * 2
-    act = T * H * 2 + 2 * T * k * H * 2 + 2 * T * k * H * 2 + T * H * 2
+    expert_bytes = 2 * H * I * gb + H * I * 2
+    shared_bytes = w.n_shared * (2 * H * w.inter_shared * gb + H * w.inter_shared * 2)
+    act = T * H * 2 + 2 * T * k * H * gb + 2 * T * k * H * 2 + T * H * 2
     B = touched * expert_bytes + shared_bytes + E * H * 2 + act
     F = 6 * H * I * T * k + 6 * H * w.inter_shared * w.n_shared * T + 2 * T * H * E
     # gate/up launch: gate+up weights of touched slots and shared, x_disp + x read, h written
-    B_gu = touched * 2 * H * I * 2 + w.n_shared * 2 * H * w.inter_shared * 2 + T * k * H * 2 + T * H * 2 + \
+    B_gu = touched * 2 * H * I * gb + w.n_shared * 2 * H * w.inter_shared * gb + T * k * H * gb + T * H * gb + \
         T * k * I * 2 + T * w.n_shared * w.inter_shared * 2
     return dict(touched=touched, bytes=B, flops=F, gate_up_bytes=B_gu)
 
@@ -165,6 +169,17 @@ def run_ours(args, rank, world, local_rank):
     wg, wu, wd = mi.stacked_expert_weights(w, rep, device=dev)
     sg, su, sd = mi.stacked_shared_weights(w, device=dev)
     mi.clear_cache()
+    fp8 = bool(args.fp8)
+    if fp8:  # E4M3 gate/up weights with one scale per output row (the bf16 copies are dropped)
+        def quant(t):
+            q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
+            sc = torch.empty(t.shape[0] * t.shape[1], dtype=torch.float32, device=dev)
+            m.moe_quantize_rows_fp8(t.view(-1, t.shape[-1]), q, sc)
+            return q, sc
+        (qg, s_g), (qu, s_u) = quant(wg), quant(wu)
+        (qsg, s_sg), (qsu, s_su) = quant(sg), quant(su)
+        del wg, wu, sg, su
+        torch.cuda.synchronize(dev)
     repd = torch.from_numpy(rep).to(dev) if rep is not None else None
     torch.cuda.empty_cache()
 
@@ -180,6 +195,11 @@ def run_ours(args, rank, world, local_rank):
     perm = torch.empty(n, **i32)
     inv = torch.empty(n, **i32)
     x_disp = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+    if fp8:
+        x8 = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        xs8 = torch.empty(T, dtype=torch.float32, device=dev)
+        x_disp8 = torch.empty((n, H), dtype=torch.uint8, device=dev)
+        xds8 = torch.empty(n, dtype=torch.float32, device=dev)
     h = torch.empty((n, I), dtype=torch.bfloat16, device=dev)
     hs = torch.empty((T, w.n_shared * w.inter_shared), dtype=torch.bfloat16, device=dev)
     y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
@@ -197,16 +217,24 @@ def run_ours(args, rank, world, local_rank):
             m.moe_route_grouped(w, T, groups[0], groups[1], x, wr, bias, None, None, idx, tw, rws)
         else:
             m.moe_route(w, T, x, wr, bias, None, None, idx, tw, rws)
-        m.moe_dispatch(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x_disp)
+        if fp8:
+            m.moe_dispatch_fp8(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x8, xs8, x_disp8,
+                               xds8)
+        else:
+            m.moe_dispatch(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x_disp)
         if ev is not None:
             ev[0].record(stream)
-        m.moe_expert_gate_up(w, T, x, x_disp, offsets, wg, wu, sg, su, h, hs)
+        if fp8:
+            m.moe_expert_gate_up_fp8(w, T, x8, xs8, x_disp8, xds8, offsets, qg, s_g, qu, s_u, qsg, s_sg, qsu, s_su,
+                                     h, hs)
+        else:
+            m.moe_expert_gate_up(w, T, x, x_disp, offsets, wg, wu, sg, su, h, hs)
         if ev is not None:
             ev[1].record(stream)
         m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh)
         m.moe_combine(w, T, y, inv, tw, ysh, out)
 
-    launches_per_step = 7
+    launches_per_step = 8 if fp8 else 7
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -246,13 +274,16 @@ def run_ours(args, rank, world, local_rank):
     x_host = x.cpu().pin_memory()
     out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     x_e2e = torch.empty_like(x)
-    ws = torch.empty(m.moe_workspace_size(w, T), dtype=torch.uint8, device=dev)
+    ws = torch.empty((m.moe_workspace_size_fp8 if fp8 else m.moe_workspace_size)(w, T), dtype=torch.uint8,
+                     device=dev)
 
     def e2e_step():
         x_e2e.copy_(x_host, non_blocking=True)
         if groups:  # the whole layer through the staged calls (moe_forward routes over all experts)
             x.copy_(x_e2e)
             step()
+        elif fp8:
+            m.moe_forward_fp8(w, T, x_e2e, wr, bias, repd, qg, s_g, qu, s_u, wd, qsg, s_sg, qsu, s_su, sd, out, ws=ws)
         else:
             m.moe_forward(w, T, x_e2e, wr, bias, repd, wg, wu, wd, sg, su, sd, out, ws=ws)
         out_host.copy_(out, non_blocking=True)
@@ -280,7 +311,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     cnt = counts.cpu().numpy()
-    bf = layer_bytes_flops(w, cnt)
+    bf = layer_bytes_flops(w, cnt, fp8)
     hbm, tf_burst, tf_sus, src = peaks()
     ms_step = elapsed_ms / args.steps
     t_roof_ms = max(bf["bytes"] / (hbm * 1e9), bf["flops"] / (tf_sus * 1e12)) * 1e3
@@ -297,7 +328,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3 gate/up + bf16" if fp8 else "bf16",
         "data": "synthetic (seeded counter-based generator; random-init DeepSeek-V3 MoE layer weights)",
         "config": {
             "workload": w.name, "description": w.description, "tokens": T, "hidden": H, "inter": I,
@@ -306,6 +337,8 @@ def run_ours(args, rank, world, local_rank):
             "l2": "inputs larger than L2: each step streams %.1f GB of touched expert weights" % (bf["bytes"] / 1e9),
             "parallelism": "replica x%d (independent layer per GPU)" % world,
             "routing": ("group-limited: %d groups, keep %d" % groups) if groups else "top-%d of all experts" % k,
+            "precision": ("E4M3 gate/up weights and dispatch payload (per-row scales), bf16 router, down and "
+                          "combine") if fp8 else "bf16 weights and activations, fp32 accumulate",
         },
         "us_per_layer": round(ms_step * 1e3, 2),
         "layer_roofline": {
@@ -314,13 +347,14 @@ def run_ours(args, rank, world, local_rank):
             "frac": round(t_roof_ms / ms_step, 4), "peaks": src,
         },
         "roofline": {
-            "kernel": "grouped_gemm_kernel<gate_up> (moe_expert_gate_up)",
+            "kernel": ("grouped_gemm_kernel<gate_up_e4m3> (moe_expert_gate_up_fp8)" if fp8
+                       else "grouped_gemm_kernel<gate_up> (moe_expert_gate_up)"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": hbm,
             "unit": "GB/s",
             "frac": round(achieved / hbm, 4),
-            "traffic": recorded_traffic("gate_up", w.name),
+            "traffic": recorded_traffic("gate_up_fp8" if fp8 else "gate_up", w.name),
             "algorithmic_bytes_per_launch": bf["gate_up_bytes"],
             "avg_launch_us": round(gu_ms * 1e3, 2),
             "peak_source": src + " (hbm_gbs, copy bandwidth)",
@@ -540,6 +574,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--route-groups", default="", help="G:Gk group-limited routing (timed region only)")
     ap.add_argument("--eplb", action="store_true", help="time the online EPLB loop instead (own JSON line)")
+    ap.add_argument("--fp8", action="store_true", help="E4M3 gate/up weights and dispatch payload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
