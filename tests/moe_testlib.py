@@ -99,7 +99,10 @@ class DeviceLayer:
         if weights is None:
             weights = mi.stacked_expert_weights(w, replica_of, device=self.dev)
         self.wg, self.wu, self.wd = weights
-        self.sg, self.su, self.sd = mi.stacked_shared_weights(w, device=self.dev)
+        if w.n_shared > 0:
+            self.sg, self.su, self.sd = mi.stacked_shared_weights(w, device=self.dev)
+        else:
+            self.sg = self.su = self.sd = None
 
     def forward(self, mode=m.MOE_FFN_AUTO):
         w, T = self.w, self.w.tokens
