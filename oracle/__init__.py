@@ -288,28 +288,96 @@ def quantize_rows_e4m3(x):
     return codes.reshape(xs.shape), scale
 
 
-def swiglu_row_fp8(qx, sx, qg, sg, qu, su, w_down) -> np.ndarray:
-    qx, qg, qu = (np.ascontiguousarray(a, np.uint8) for a in (qx, qg, qu))
-    sg, su = _f32(sg), _f32(su)
-    d = _u16(w_down)
+def bf16_round(values) -> np.ndarray:
+    """Nearest bf16 (ties to even) of each value, as uint16 bit patterns."""
+    f = lib().oracle_double_to_bf16
+    f.restype = ctypes.c_uint16
+    f.argtypes = [ctypes.c_double]
+    v = np.asarray(values, dtype=np.float64)
+    return np.array([f(float(a)) for a in v.ravel()], dtype=np.uint16).reshape(v.shape)
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, np.uint8)
+
+
+def gate_up_row_fp8(qx, sx, qg, sg, qu, su) -> np.ndarray:
+    """h = silu(g) * u of one row from E4M3 codes (qg/qu [I, H]) and scales."""
+    qg, qu = _u8(qg), _u8(qu)
     I, H = qg.shape
+    h = np.empty(I, dtype=np.float64)
+    lib().oracle_gate_up_row_fp8(H, I, _ptr(_u8(qx)), ctypes.c_float(float(sx)), _ptr(qg), _ptr(_f32(sg)), _ptr(qu),
+                                 _ptr(_f32(su)), _ptr(h))
+    return h
+
+
+def down_row_fp8(qh, sh, qd, sd) -> np.ndarray:
+    """y[o] = sh * sd[o] * sum_i qh_i * qd[o, i] over decoded E4M3 codes (qd [H, K])."""
+    qd = _u8(qd)
+    H, K = qd.shape
     y = np.empty(H, dtype=np.float64)
-    lib().oracle_swiglu_row_fp8(H, I, _ptr(qx), ctypes.c_float(float(sx)), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su),
-                                _ptr(d), _ptr(y))
+    lib().oracle_down_row_fp8(K, H, _ptr(_u8(qh)), ctypes.c_float(float(sh)), _ptr(qd), _ptr(_f32(sd)), _ptr(y))
     return y
 
 
-def moe_forward_fp8(w, x, w_router, bias, replica_of, q, ws_down_bf16):
-    """Layer with FP8 payload and FP8 gate/up; q = dict(qg, sg, qu, su, wd, qsg, ssg, qsu, ssu)."""
+def swiglu_row_fp8(qx, sx, qg, sg, qu, su, qd, sd) -> np.ndarray:
+    """One routed expert on one token in FP8 (gate/up, h -> bf16 -> E4M3 row, down)."""
+    qg, qu, qd = _u8(qg), _u8(qu), _u8(qd)
+    I, H = qg.shape
+    y = np.empty(H, dtype=np.float64)
+    lib().oracle_swiglu_row_fp8(H, I, _ptr(_u8(qx)), ctypes.c_float(float(sx)), _ptr(qg), _ptr(_f32(sg)), _ptr(qu),
+                                _ptr(_f32(su)), _ptr(qd), _ptr(_f32(sd)), _ptr(y))
+    return y
+
+
+def shared_row_fp8(w, qx, sx, q) -> np.ndarray:
+    """Sum of the shared experts on one token in FP8; q holds qsg, ssg, qsu, ssu, qsd, ssd."""
+    y = np.empty(w.hidden, dtype=np.float64)
+    lib().oracle_shared_row_fp8(ctypes.byref(shape_of(w)), _ptr(_u8(qx)), ctypes.c_float(float(sx)),
+                                _ptr(_u8(q["qsg"])), _ptr(_f32(q["ssg"])), _ptr(_u8(q["qsu"])), _ptr(_f32(q["ssu"])),
+                                _ptr(_u8(q["qsd"])), _ptr(_f32(q["ssd"])), _ptr(y))
+    return y
+
+
+def shared_down_matrix(ws_down):
+    """The shared experts' down weights [n_sh, H, I_sh] as one matrix [H, n_sh*I_sh]
+    (expert j's columns at j*I_sh): the shared outputs are summed, so this
+    matrix times the concatenated intermediate is their sum."""
+    n_sh, H, Is = ws_down.shape
+    return ws_down.permute(1, 0, 2).reshape(H, n_sh * Is).contiguous()
+
+
+def quantize_layer_fp8(w, w_gate, w_up, w_down, ws_gate, ws_up, ws_down) -> dict:
+    """E4M3 codes and per-output-row scales of every expert matrix of the FP8
+    layer: routed gate/up [S*I, H] rows, routed down [S*H, I] rows, shared
+    gate/up [n_sh*I_sh, H] rows, shared down as one [H, n_sh*I_sh] matrix."""
+    H, I = w.hidden, w.inter
+    q = {}
+    q["qg"], q["sg"] = quantize_rows_e4m3(w_gate.reshape(-1, H))
+    q["qu"], q["su"] = quantize_rows_e4m3(w_up.reshape(-1, H))
+    q["qd"], q["sd"] = quantize_rows_e4m3(w_down.reshape(-1, I))
+    if w.n_shared > 0:
+        q["qsg"], q["ssg"] = quantize_rows_e4m3(ws_gate.reshape(-1, H))
+        q["qsu"], q["ssu"] = quantize_rows_e4m3(ws_up.reshape(-1, H))
+        q["qsd"], q["ssd"] = quantize_rows_e4m3(shared_down_matrix(ws_down))
+    else:
+        for k_, dt in (("qsg", np.uint8), ("qsu", np.uint8), ("qsd", np.uint8)):
+            q[k_] = np.zeros(16, dt)
+        for k_ in ("ssg", "ssu", "ssd"):
+            q[k_] = np.ones(16, np.float32)
+    return q
+
+
+def moe_forward_fp8(w, x, w_router, bias, replica_of, q):
+    """Layer in FP8 (payload and every expert matrix); q as quantize_layer_fp8 returns."""
     T = x.shape[0]
     idx = np.empty((T, w.top_k), np.int32)
     out = np.empty((T, w.hidden), np.float64)
-    arr = [np.ascontiguousarray(q[k], np.uint8 if k.startswith("q") else np.float32)
-           for k in ("qg", "sg", "qu", "su")]
-    sh = [np.ascontiguousarray(q[k], np.uint8 if k.startswith("q") else np.float32)
-          for k in ("qsg", "ssg", "qsu", "ssu")]
+    a = {k_: (_u8(q[k_]) if k_.startswith("q") else _f32(q[k_]))
+         for k_ in ("qg", "sg", "qu", "su", "qd", "sd", "qsg", "ssg", "qsu", "ssu", "qsd", "ssd")}
     inv = lib().oracle_moe_forward_fp8(
         ctypes.byref(shape_of(w)), T, _ptr(_u16(x)), _ptr(_u16(w_router)), _ptr(_f32(bias)),
-        _ptr(_i32(replica_of)), _ptr(arr[0]), _ptr(arr[1]), _ptr(arr[2]), _ptr(arr[3]), _ptr(_u16(q["wd"])),
-        _ptr(sh[0]), _ptr(sh[1]), _ptr(sh[2]), _ptr(sh[3]), _ptr(_u16(ws_down_bf16)), _ptr(idx), _ptr(out))
+        _ptr(_i32(replica_of)), *(_ptr(a[k_]) for k_ in ("qg", "sg", "qu", "su", "qd", "sd", "qsg", "ssg", "qsu",
+                                                        "ssu", "qsd", "ssd")),
+        _ptr(idx), _ptr(out))
     return dict(idx=idx, out=out, invalid=inv)

@@ -466,9 +466,22 @@ void oracle_quantize_rows_e4m3(int rows, int cols, const uint16_t* x_bf16, uint8
     }
 }
 
-void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
-                           const uint8_t* qu, const float* su, const uint16_t* w_down, double* y) {
-    double* h = (double*)malloc((size_t)I * sizeof(double));
+uint16_t oracle_double_to_bf16(double v) {
+    if (isnan(v)) return 0x7FC0;
+    if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+    int ex;
+    frexp(fabs(v), &ex);         /* |v| in [2^(ex-1), 2^ex) */
+    if (ex < -125) ex = -125;    /* below 2^-126 the grid stays at 2^-133 (subnormals) */
+    const double step = ldexp(1.0, ex - 8);   /* 8 significant bits */
+    const double r = rint(v / step) * step;   /* nearest multiple, ties to even */
+    const float f = (float)r;                 /* exact (or +-inf past the largest bf16) */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(bits >> 16);
+}
+
+void oracle_gate_up_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
+                            const uint8_t* qu, const float* su, double* h) {
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int c = 0; c < H; ++c) {
@@ -480,21 +493,60 @@ void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint
         u *= (double)sx * (double)su[i];
         h[i] = silu(g) * u;
     }
+}
+
+void oracle_down_row_fp8(int K, int H, const uint8_t* qh, float sh, const uint8_t* qd, const float* sd, double* y) {
     for (int o = 0; o < H; ++o) {
         double acc = 0.0;
-        for (int i = 0; i < I; ++i) acc += h[i] * oracle_bf16_to_double(w_down[(size_t)o * I + i]);
-        y[o] = acc;
+        for (int i = 0; i < K; ++i) acc += oracle_e4m3_decode(qh[i]) * oracle_e4m3_decode(qd[(size_t)o * K + i]);
+        y[o] = acc * (double)sh * (double)sd[o];
     }
-    free(h);
+}
+
+/* h (fp64) -> bf16 -> one E4M3 row with its scale */
+static void quantize_h_row(int K, const double* h, uint16_t* hb, uint8_t* qh, float* sh) {
+    for (int i = 0; i < K; ++i) hb[i] = oracle_double_to_bf16(h[i]);
+    oracle_quantize_rows_e4m3(1, K, hb, qh, sh);
+}
+
+void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
+                           const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd, double* y) {
+    double* h = (double*)malloc((size_t)I * sizeof(double));
+    uint16_t* hb = (uint16_t*)malloc((size_t)I * sizeof(uint16_t));
+    uint8_t* qh = (uint8_t*)malloc((size_t)I);
+    float sh;
+    oracle_gate_up_row_fp8(H, I, qx, sx, qg, sg, qu, su, h);
+    quantize_h_row(I, h, hb, qh, &sh);
+    oracle_down_row_fp8(I, H, qh, sh, qd, sd, y);
+    free(h); free(hb); free(qh);
+}
+
+void oracle_shared_row_fp8(const oracle_shape* s, const uint8_t* qx, float sx, const uint8_t* qsg, const float* ssg,
+                           const uint8_t* qsu, const float* ssu, const uint8_t* qsd, const float* ssd, double* y) {
+    const int H = s->hidden, Is = s->inter_shared, n_sh = s->n_shared;
+    const int K = n_sh * Is;
+    if (n_sh == 0) {
+        for (int o = 0; o < H; ++o) y[o] = 0.0;
+        return;
+    }
+    double* h = (double*)malloc((size_t)K * sizeof(double));
+    uint16_t* hb = (uint16_t*)malloc((size_t)K * sizeof(uint16_t));
+    uint8_t* qh = (uint8_t*)malloc((size_t)K);
+    float sh;
+    for (int j = 0; j < n_sh; ++j)
+        oracle_gate_up_row_fp8(H, Is, qx, sx, qsg + (size_t)j * Is * H, ssg + (size_t)j * Is, qsu + (size_t)j * Is * H,
+                               ssu + (size_t)j * Is, h + (size_t)j * Is);
+    quantize_h_row(K, h, hb, qh, &sh);
+    oracle_down_row_fp8(K, H, qh, sh, qsd, ssd, y);
+    free(h); free(hb); free(qh);
 }
 
 int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
                            const float* bias, const int32_t* replica_of, const uint8_t* qg, const float* sg,
-                           const uint8_t* qu, const float* su, const uint16_t* w_down, const uint8_t* qsg,
-                           const float* ssg, const uint8_t* qsu, const float* ssu, const uint16_t* ws_down,
-                           int32_t* idx, double* out) {
+                           const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd,
+                           const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
+                           const uint8_t* qsd, const float* ssd, int32_t* idx, double* out) {
     const int H = s->hidden, E = s->n_experts, k = s->top_k, S = s->n_slots, I = s->inter;
-    const int Is = s->inter_shared;
     const size_t n = (size_t)T * k;
     double* logits = (double*)malloc((size_t)T * E * sizeof(double));
     double* w = (double*)malloc(n * sizeof(double));
@@ -507,7 +559,6 @@ int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, cons
     float* sx = (float*)malloc((size_t)T * sizeof(float));
     double* yd = (double*)calloc(n * H, sizeof(double));
     double* ysh = (double*)calloc((size_t)T * H, sizeof(double));
-    double* tmp = (double*)malloc((size_t)H * sizeof(double));
 
     oracle_router_logits(s, T, x, w_router, bias, logits);
     oracle_topk_softmax(T, E, k, logits, idx, w);
@@ -519,19 +570,14 @@ int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, cons
         for (int row = off[slot]; row < off[slot + 1]; ++row) {
             const int t = perm[row] / k;
             oracle_swiglu_row_fp8(H, I, qx + (size_t)t * H, sx[t], qg + (size_t)slot * I * H, sg + (size_t)slot * I,
-                                  qu + (size_t)slot * I * H, su + (size_t)slot * I, w_down + (size_t)slot * H * I,
-                                  yd + (size_t)row * H);
+                                  qu + (size_t)slot * I * H, su + (size_t)slot * I, qd + (size_t)slot * H * I,
+                                  sd + (size_t)slot * H, yd + (size_t)row * H);
         }
     }
-    for (int t = 0; t < T; ++t) {
-        for (int j = 0; j < s->n_shared; ++j) {
-            oracle_swiglu_row_fp8(H, Is, qx + (size_t)t * H, sx[t], qsg + (size_t)j * Is * H, ssg + (size_t)j * Is,
-                                  qsu + (size_t)j * Is * H, ssu + (size_t)j * Is, ws_down + (size_t)j * H * Is, tmp);
-            for (int o = 0; o < H; ++o) ysh[(size_t)t * H + o] += tmp[o];
-        }
-    }
+    for (int t = 0; t < T; ++t)
+        oracle_shared_row_fp8(s, qx + (size_t)t * H, sx[t], qsg, ssg, qsu, ssu, qsd, ssd, ysh + (size_t)t * H);
     oracle_combine(s, T, yd, inv, w, ysh, out);
     free(logits); free(w); free(so); free(cnt); free(off); free(perm); free(inv);
-    free(qx); free(sx); free(yd); free(ysh); free(tmp);
+    free(qx); free(sx); free(yd); free(ysh);
     return invalid;
 }

@@ -155,23 +155,47 @@ double oracle_e4m3_decode(uint8_t code);
  * Dequantised value = decode(code) * scale. */
 void oracle_quantize_rows_e4m3(int rows, int cols, const uint16_t* x_bf16, uint8_t* codes, float* scale);
 
-/* FFN of one row with FP8 gate/up: g_i = sx*sg[i] * sum_c qx_c*qg[i][c] (exact
- * products of dequantised values in fp64), u likewise, h = silu(g)*u,
- * y = h W_d^T with the bf16 down weights.  qg/qu [I,H] codes, sg/su [I]. */
-void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
-                           const uint8_t* qu, const float* su, const uint16_t* w_down, double* y);
+/* bf16 value nearest to v (ties to even), as a bit pattern.  The layer keeps
+ * the SwiGLU intermediate h in bf16, so the FP8 down projection quantises the
+ * bf16 h. */
+uint16_t oracle_double_to_bf16(double v);
 
-/* Whole layer with the FP8 dispatch payload and FP8 gate/up weights: routing
- * as oracle_moe_forward (bf16 router), every token quantised once per row
- * (its k dispatched copies carry the same codes and scale), routed and shared
- * gate/up in FP8 (codes qg/qu [S,I,H] with scales [S,I]; shared [n_sh,I_sh,H]
- * with [n_sh,I_sh]), down projections in bf16, combine as oracle_combine.
- * Returns the number of invalid expert ids. */
+/* FP8 gate/up of one row: g_i = sx*sg[i] * sum_c qx_c*qg[i][c] (exact products
+ * of decoded values in fp64), u likewise, h_i = silu(g_i)*u_i.  qg/qu [I,H]. */
+void oracle_gate_up_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
+                            const uint8_t* qu, const float* su, double* h);
+
+/* FP8 down projection of one row: y[o] = sh*sd[o] * sum_i qh_i*qd[o][i]
+ * (decoded values), qh [K] codes of the intermediate with scale sh,
+ * qd [H,K] codes with one scale per output row sd [H]. */
+void oracle_down_row_fp8(int K, int H, const uint8_t* qh, float sh, const uint8_t* qd, const float* sd, double* y);
+
+/* One routed expert on one token, all in FP8: oracle_gate_up_row_fp8, h
+ * rounded to bf16 and quantised as one row (oracle_quantize_rows_e4m3), then
+ * oracle_down_row_fp8.  qd [H,I] codes, sd [H]. */
+void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint8_t* qg, const float* sg,
+                           const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd, double* y);
+
+/* The shared experts on one token in FP8.  Their outputs are summed, so their
+ * down matrices act as one matrix [H, n_sh*I_sh] (expert j's columns at
+ * j*I_sh) applied to the concatenated intermediate [n_sh*I_sh]; that matrix
+ * has one scale per output row (ssd [H]) and the concatenated intermediate
+ * (bf16, as for a routed row) one scale per token.  qsg/qsu [n_sh,I_sh,H],
+ * ssg/ssu [n_sh*I_sh], qsd [H, n_sh*I_sh]. */
+void oracle_shared_row_fp8(const oracle_shape* s, const uint8_t* qx, float sx, const uint8_t* qsg, const float* ssg,
+                           const uint8_t* qsu, const float* ssu, const uint8_t* qsd, const float* ssd, double* y);
+
+/* Whole layer in FP8: routing as oracle_moe_forward (bf16 router), every
+ * token quantised once per row (its k dispatched copies carry the same codes
+ * and scale), routed experts by oracle_swiglu_row_fp8 (qg/qu [S,I,H] with
+ * scales [S*I], qd [S,H,I] with [S*H]), shared experts by
+ * oracle_shared_row_fp8, combine as oracle_combine.  Returns the number of
+ * invalid expert ids. */
 int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
                            const float* bias, const int32_t* replica_of, const uint8_t* qg, const float* sg,
-                           const uint8_t* qu, const float* su, const uint16_t* w_down, const uint8_t* qsg,
-                           const float* ssg, const uint8_t* qsu, const float* ssu, const uint16_t* ws_down,
-                           int32_t* idx, double* out);
+                           const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd,
+                           const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
+                           const uint8_t* qsd, const float* ssd, int32_t* idx, double* out);
 
 /* Replica placement for n_rep redundant slots from per-expert counts[E].
  * Hot list: the n_rep experts with the largest counts (ties -> lower id).

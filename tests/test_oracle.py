@@ -505,53 +505,119 @@ def test_row_quantizer_scale_and_error_bound():
     assert np.all(err[~normal] <= 2.0 ** -10 * scale[:, None].repeat(96, 1)[~normal] * 1.0000001)
 
 
-def test_fp8_swiglu_row_reduces_to_bf16_on_exact_values():
+def test_bf16_rounding_of_doubles():
+    rng = np.random.default_rng(11)
+    # float32 inputs: one rounding, so torch's float32 -> bf16 conversion is the reference
+    xs = np.concatenate([rng.normal(0, 1, 3000), rng.normal(0, 1e-30, 200), rng.uniform(-3e38, 3e38, 200)])
+    xs = xs.astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_round(xs.astype(np.float64)), ref)
+    # ties to even, and a value just above a tie that float32 cannot hold
+    one = 1.0
+    cases = [(one, 0x3F80), (one + 2.0 ** -8, 0x3F80), (one + 3 * 2.0 ** -8, 0x3F82),
+             (one + 2.0 ** -8 + 2.0 ** -40, 0x3F81), (-(one + 2.0 ** -8 + 2.0 ** -40), 0xBF81), (0.0, 0x0000),
+             (-0.0, 0x8000), (2.0 ** -133, 0x0001), (3 * 2.0 ** -134, 0x0002), (2.0 ** -134, 0x0000)]
+    got = oracle.bf16_round([v for v, _ in cases])
+    assert [int(v) for v in got] == [b for _, b in cases]
+
+
+def _e4m3_values(codes):
+    """Decode through torch's float8_e4m3fn type (a library routine)."""
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(torch.float64)
+
+
+def _random_codes(rng, shape):
+    c = rng.integers(0, 256, shape).astype(np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    return c
+
+
+def test_fp8_down_row_is_a_scaled_product_of_decoded_codes():
+    rng = np.random.default_rng(12)
+    K, H = 40, 24  # not square, so a transposed operand cannot pass
+    qh, qd = _random_codes(rng, K), _random_codes(rng, (H, K))
+    sh = np.float32(0.375)
+    sd = (2.0 ** rng.integers(-4, 4, H)).astype(np.float32) * np.float32(1.25)
+    y = oracle.down_row_fp8(qh, sh, qd, sd)
+    ref = (_e4m3_values(qd) @ _e4m3_values(qh)) * float(sh) * torch.from_numpy(sd.astype(np.float64))
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-15, atol=0)
+
+
+def test_fp8_gate_up_row_reduces_to_bf16_on_exact_values():
     rng = np.random.default_rng(4)
     H, I = 48, 24
     grid = np.array([0.0, 0.25, 0.5, 0.75, 1.0, 1.5, 2.0, -0.25, -0.5, -1.0, -1.5, -2.0])
     xv, gv, uv = rng.choice(grid, H), rng.choice(grid, (I, H)) / 4, rng.choice(grid, (I, H)) / 4
-    d = _bf16((H, I), I ** -0.5, 5, 5)
-    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16)
-    y8 = oracle.swiglu_row_fp8(oracle.e4m3_encode(xv), 1.0, oracle.e4m3_encode(gv).reshape(I, H), np.ones(I),
-                               oracle.e4m3_encode(uv).reshape(I, H), np.ones(I), d)
-    y = oracle.swiglu_row(to_bf16(xv), to_bf16(gv), to_bf16(uv), d)
-    np.testing.assert_allclose(y8, y, rtol=1e-13, atol=1e-15)
-    # scales factor out of the sums
-    y8s = oracle.swiglu_row_fp8(oracle.e4m3_encode(xv), 2.0, oracle.e4m3_encode(gv).reshape(I, H), np.full(I, 0.5),
-                                oracle.e4m3_encode(uv).reshape(I, H), np.full(I, 0.25), d)
-    y2 = oracle.swiglu_row(to_bf16(xv), to_bf16(gv), to_bf16(uv / 2), d)
-    np.testing.assert_allclose(y8s, y2, rtol=1e-13, atol=1e-15)
+    t64 = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    want = (F.silu(t64(gv) @ t64(xv)) * (t64(uv) @ t64(xv))).numpy()
+    h = oracle.gate_up_row_fp8(oracle.e4m3_encode(xv), 1.0, oracle.e4m3_encode(gv).reshape(I, H), np.ones(I),
+                               oracle.e4m3_encode(uv).reshape(I, H), np.ones(I))
+    np.testing.assert_allclose(h, want, rtol=1e-14, atol=1e-15)
+    # scales factor out of the sums: x scale 2, gate rows 0.5, up rows 0.25 -> u halved
+    hs = oracle.gate_up_row_fp8(oracle.e4m3_encode(xv), 2.0, oracle.e4m3_encode(gv).reshape(I, H), np.full(I, 0.5),
+                                oracle.e4m3_encode(uv).reshape(I, H), np.full(I, 0.25))
+    np.testing.assert_allclose(hs, want / 2, rtol=1e-14, atol=1e-15)
 
 
-def _fp8_weights(w, wg, wu, wd, sg_, su_, sd_):
-    qg, sgs = oracle.quantize_rows_e4m3(wg.reshape(-1, w.hidden))
-    qu, sus = oracle.quantize_rows_e4m3(wu.reshape(-1, w.hidden))
-    qsg, ssg = oracle.quantize_rows_e4m3(sg_.reshape(-1, w.hidden))
-    qsu, ssu = oracle.quantize_rows_e4m3(su_.reshape(-1, w.hidden))
-    return dict(qg=qg, sg=sgs, qu=qu, su=sus, wd=wd, qsg=qsg, ssg=ssg, qsu=qsu, ssu=ssu)
+def _quantise_torch(rows_bf16):
+    """Per-row E4M3 with torch: fp32 scale amax/448 (1 for a zero row), torch's fp8 conversion."""
+    xf = rows_bf16.float()
+    amax = xf.abs().amax(-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    return (xf / scale).to(torch.float8_e4m3fn).to(torch.float64) * scale.double()
+
+
+def test_fp8_expert_row_is_gate_up_then_bf16_row_quantised_down():
+    H, I = 64, 48
+    x = _bf16((1, H), 1.0, 3, 7)
+    g, u = _bf16((I, H), H ** -0.5, 3, 8), _bf16((I, H), H ** -0.5, 3, 9)
+    d = _bf16((H, I), I ** -0.5, 3, 10)
+    (qx, sx), (qg, sg), (qu, su), (qd, sd) = (oracle.quantize_rows_e4m3(t) for t in (x, g, u, d))
+    y = oracle.swiglu_row_fp8(qx[0], sx[0], qg, sg, qu, su, qd, sd)
+    deq = lambda c, s_: _e4m3_values(c) * torch.from_numpy(s_.astype(np.float64))[:, None]
+    xq, G, U, D = deq(qx, sx), deq(qg, sg), deq(qu, su), deq(qd, sd)
+    h = F.silu(F.linear(xq, G)) * F.linear(xq, U)
+    hq = _quantise_torch(h.to(torch.bfloat16))
+    np.testing.assert_allclose(y, F.linear(hq, D)[0].numpy(), rtol=1e-12, atol=1e-14)
+    # the down step alone, on the same intermediate
+    qh, shs = oracle.quantize_rows_e4m3(h.to(torch.bfloat16))
+    np.testing.assert_allclose(y, oracle.down_row_fp8(qh[0], shs[0], qd, sd), rtol=1e-15, atol=0)
+
+
+def test_shared_down_matrix_layout():
+    sd = _bf16((3, 8, 5), 1.0, 3, 11)
+    m = oracle.shared_down_matrix(sd)
+    for j in range(3):
+        assert torch.equal(m[:, 5 * j:5 * (j + 1)], sd[j])
 
 
 def test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors():
     w = _tiny(top_k=3, n_shared=2, inter_shared=24, tokens=21)
     x, wr, _, wg, wu, wd, sg, su, sd = _tiny_inputs(w)
-    q = _fp8_weights(w, wg, wu, wd, sg, su, sd)
-    r = oracle.moe_forward_fp8(w, x, wr, None, None, q, sd)
+    q = oracle.quantize_layer_fp8(w, wg, wu, wd, sg, su, sd)
+    r = oracle.moe_forward_fp8(w, x, wr, None, None, q)
     deq = lambda c, s_: torch.from_numpy(oracle.e4m3_decode(c).reshape(c.shape) * s_[:, None].astype(np.float64))
     qx, sx = oracle.quantize_rows_e4m3(x)
     xq = deq(qx, sx)
     G = deq(q["qg"], q["sg"]).reshape(w.n_experts, w.inter, w.hidden)
     U = deq(q["qu"], q["su"]).reshape(w.n_experts, w.inter, w.hidden)
+    D = deq(q["qd"], q["sd"]).reshape(w.n_experts, w.hidden, w.inter)
     SG = deq(q["qsg"], q["ssg"]).reshape(w.n_shared, w.inter_shared, w.hidden)
     SU = deq(q["qsu"], q["ssu"]).reshape(w.n_shared, w.inter_shared, w.hidden)
+    SD = deq(q["qsd"], q["ssd"])  # [H, n_sh * I_sh]
+    Is = w.inter_shared
+    for j in range(w.n_shared):  # each shared expert's columns hold its own down weights
+        assert torch.allclose(SD[:, j * Is:(j + 1) * Is], _f64(sd[j]), rtol=2.0 ** -4, atol=1e-3)
     logits = _f64(x) @ _f64(wr).T
     p = torch.softmax(logits, -1)
     top = torch.topk(logits, w.top_k, -1).indices
     ref = torch.zeros(w.tokens, w.hidden, dtype=torch.float64)
     for e in range(w.n_experts):
-        y = F.linear(F.silu(F.linear(xq, G[e])) * F.linear(xq, U[e]), _f64(wd[e]))
+        h = F.silu(F.linear(xq, G[e])) * F.linear(xq, U[e])
+        y = F.linear(_quantise_torch(h.to(torch.bfloat16)), D[e])
         ref += ((top == e).any(-1).double() * p[:, e])[:, None] * y
-    for j in range(w.n_shared):
-        ref += F.linear(F.silu(F.linear(xq, SG[j])) * F.linear(xq, SU[j]), _f64(sd[j]))
+    hsh = torch.cat([F.silu(F.linear(xq, SG[j])) * F.linear(xq, SU[j]) for j in range(w.n_shared)], -1)
+    ref += F.linear(_quantise_torch(hsh.to(torch.bfloat16)), SD)
     assert np.array_equal(np.sort(r["idx"], 1), np.sort(top.numpy(), 1))
     np.testing.assert_allclose(r["out"], ref.numpy(), rtol=1e-11, atol=1e-12 * ref.abs().max().item())
     # and it stays close to the bf16 layer

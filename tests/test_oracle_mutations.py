@@ -46,6 +46,10 @@ MUTANTS = [
     ("row scale uses the wrong maximum", "const float s = amax > 0.0f ? amax / 448.0f : 1.0f;",
      "const float s = amax > 0.0f ? amax / 240.0f : 1.0f;"),
     ("fp8 gate ignores the token scale", "g *= (double)sx * (double)sg[i];", "g *= (double)sg[i];"),
+    ("fp8 down ignores the weight-row scale", "y[o] = acc * (double)sh * (double)sd[o];", "y[o] = acc * (double)sh;"),
+    ("fp8 down reads its weights transposed", "oracle_e4m3_decode(qd[(size_t)o * K + i]);",
+     "oracle_e4m3_decode(qd[(size_t)i * H + o]);"),
+    ("bf16 rounding truncates", "const double r = rint(v / step) * step;", "const double r = trunc(v / step) * step;"),
     ("home slot ignores the replica slots", "return (e / epb) * spb + (e % epb);", "return e;"),
     ("replica used by even tokens", "replica_of[e] >= 0 && (t % 2) == 1", "replica_of[e] >= 0 && (t % 2) == 0"),
     ("dispatch fills slots in reverse order", "for (int a = 0; a < n; ++a) {\n        const int32_t slot = slot_of[a];",
@@ -90,7 +94,10 @@ PINS = [
     pins.test_e4m3_round_trip_and_monotone,
     pins.test_e4m3_encoder_matches_torch_conversion,
     pins.test_row_quantizer_scale_and_error_bound,
-    pins.test_fp8_swiglu_row_reduces_to_bf16_on_exact_values,
+    pins.test_bf16_rounding_of_doubles,
+    pins.test_fp8_down_row_is_a_scaled_product_of_decoded_codes,
+    pins.test_fp8_gate_up_row_reduces_to_bf16_on_exact_values,
+    pins.test_fp8_expert_row_is_gate_up_then_bf16_row_quantised_down,
     pins.test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors,
     pins.test_eplb_window_hand_case,
     pins.test_eplb_window_matches_histograms_of_recent_batches,
