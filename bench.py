@@ -130,13 +130,13 @@ class ClockSampler:
 def layer_bytes_flops(w, counts_np, fp8=False):
     """Algorithmic bytes and flops of one layer pass (touched expert weights read once).
 
-    fp8: gate/up weights and the dispatch payload are one byte per element.
+    fp8: expert weights and the dispatch payload are one byte per element.
     """
     H, I, E, k, T = w.hidden, w.inter, w.n_experts, w.top_k, w.tokens
-    gb = 1 if fp8 else 2  # bytes per gate/up weight and per dispatched element
+    gb = 1 if fp8 else 2  # bytes per expert weight and per dispatched element
     touched = int((counts_np[:w.n_slots] > 0).sum())
-    expert_bytes = 2 * H * I * gb + H * I * 2
-    shared_bytes = w.n_shared * (2 * H * w.inter_shared * gb + H * w.inter_shared * 2)
+    expert_bytes = 3 * H * I * gb
+    shared_bytes = w.n_shared * 3 * H * w.inter_shared * gb
     act = T * H * 2 + 2 * T * k * H * gb + 2 * T * k * H * 2 + T * H * 2
     B = touched * expert_bytes + shared_bytes + E * H * 2 + act
     F = 6 * H * I * T * k + 6 * H * w.inter_shared * w.n_shared * T + 2 * T * H * E
@@ -170,15 +170,17 @@ def run_ours(args, rank, world, local_rank):
     sg, su, sd = mi.stacked_shared_weights(w, device=dev)
     mi.clear_cache()
     fp8 = bool(args.fp8)
-    if fp8:  # E4M3 gate/up weights with one scale per output row (the bf16 copies are dropped)
+    if fp8:  # E4M3 expert weights with one scale per output row (the bf16 copies are dropped)
         def quant(t):
             q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
-            sc = torch.empty(t.shape[0] * t.shape[1], dtype=torch.float32, device=dev)
+            sc = torch.empty(t.numel() // t.shape[-1], dtype=torch.float32, device=dev)
             m.moe_quantize_rows_fp8(t.view(-1, t.shape[-1]), q, sc)
             return q, sc
-        (qg, s_g), (qu, s_u) = quant(wg), quant(wu)
+        (qg, s_g), (qu, s_u), (qd, s_d) = quant(wg), quant(wu), quant(wd)
         (qsg, s_sg), (qsu, s_su) = quant(sg), quant(su)
-        del wg, wu, sg, su
+        # the shared experts' down matrices as one [H, n_sh*I_sh] matrix (their outputs are summed)
+        qsd, s_sd = quant(sd.permute(1, 0, 2).reshape(w.hidden, -1).contiguous())
+        del wg, wu, wd, sg, su, sd
         torch.cuda.synchronize(dev)
     repd = torch.from_numpy(rep).to(dev) if rep is not None else None
     torch.cuda.empty_cache()
@@ -200,6 +202,10 @@ def run_ours(args, rank, world, local_rank):
         xs8 = torch.empty(T, dtype=torch.float32, device=dev)
         x_disp8 = torch.empty((n, H), dtype=torch.uint8, device=dev)
         xds8 = torch.empty(n, dtype=torch.float32, device=dev)
+        h8 = torch.empty((n, I), dtype=torch.uint8, device=dev)
+        h8s = torch.empty(n, dtype=torch.float32, device=dev)
+        hs8 = torch.empty((T, w.n_shared * w.inter_shared), dtype=torch.uint8, device=dev)
+        hs8s = torch.empty(T, dtype=torch.float32, device=dev)
     h = torch.empty((n, I), dtype=torch.bfloat16, device=dev)
     hs = torch.empty((T, w.n_shared * w.inter_shared), dtype=torch.bfloat16, device=dev)
     y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
@@ -231,10 +237,16 @@ def run_ours(args, rank, world, local_rank):
             m.moe_expert_gate_up(w, T, x, x_disp, offsets, wg, wu, sg, su, h, hs)
         if ev is not None:
             ev[1].record(stream)
-        m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh)
+        if fp8:
+            m.moe_quantize_rows_fp8(h, h8, h8s)
+            if w.n_shared:
+                m.moe_quantize_rows_fp8(hs, hs8, hs8s)
+            m.moe_expert_down_fp8(w, T, h8, h8s, hs8, hs8s, offsets, qd, s_d, qsd, s_sd, y, ysh)
+        else:
+            m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh)
         m.moe_combine(w, T, y, inv, tw, ysh, out)
 
-    launches_per_step = 8 if fp8 else 7
+    launches_per_step = (9 + (w.n_shared > 0)) if fp8 else 7
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -283,7 +295,8 @@ def run_ours(args, rank, world, local_rank):
             x.copy_(x_e2e)
             step()
         elif fp8:
-            m.moe_forward_fp8(w, T, x_e2e, wr, bias, repd, qg, s_g, qu, s_u, wd, qsg, s_sg, qsu, s_su, sd, out, ws=ws)
+            m.moe_forward_fp8(w, T, x_e2e, wr, bias, repd, qg, s_g, qu, s_u, qd, s_d, qsg, s_sg, qsu, s_su, qsd, s_sd,
+                              out, ws=ws)
         else:
             m.moe_forward(w, T, x_e2e, wr, bias, repd, wg, wu, wd, sg, su, sd, out, ws=ws)
         out_host.copy_(out, non_blocking=True)
@@ -328,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 gate/up + bf16" if fp8 else "bf16",
+        "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded counter-based generator; random-init DeepSeek-V3 MoE layer weights)",
         "config": {
             "workload": w.name, "description": w.description, "tokens": T, "hidden": H, "inter": I,
@@ -337,8 +350,9 @@ def run_ours(args, rank, world, local_rank):
             "l2": "inputs larger than L2: each step streams %.1f GB of touched expert weights" % (bf["bytes"] / 1e9),
             "parallelism": "replica x%d (independent layer per GPU)" % world,
             "routing": ("group-limited: %d groups, keep %d" % groups) if groups else "top-%d of all experts" % k,
-            "precision": ("E4M3 gate/up weights and dispatch payload (per-row scales), bf16 router, down and "
-                          "combine") if fp8 else "bf16 weights and activations, fp32 accumulate",
+            "precision": ("E4M3 expert weights (gate, up, down; shared included), dispatch payload and SwiGLU "
+                          "intermediate, per-row scales, fp32 accumulate; bf16 router, expert outputs and combine")
+            if fp8 else "bf16 weights and activations, fp32 accumulate",
         },
         "us_per_layer": round(ms_step * 1e3, 2),
         "layer_roofline": {
@@ -364,7 +378,8 @@ def run_ours(args, rank, world, local_rank):
             "unit": "tokens/s",
             "h2d_bytes_per_step": T * H * 2,
             "d2h_bytes_per_step": T * H * 2,
-            "api": "moe_forward (C ABI) with pinned host input/output copies in the timed region",
+            "api": ("moe_forward_fp8" if fp8 else "moe_forward") +
+                   " (C ABI) with pinned host input/output copies in the timed region",
         },
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -574,7 +589,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--route-groups", default="", help="G:Gk group-limited routing (timed region only)")
     ap.add_argument("--eplb", action="store_true", help="time the online EPLB loop instead (own JSON line)")
-    ap.add_argument("--fp8", action="store_true", help="E4M3 gate/up weights and dispatch payload")
+    ap.add_argument("--fp8", action="store_true", help="E4M3 expert weights and dispatch payload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

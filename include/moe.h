@@ -302,11 +302,22 @@ MOE_API int moe_expert_ffn_noalloc(const moe_shape_t* shape, int T, const void* 
  * T*k*H bytes, half of the bf16 one (57,344 B per token at k=8, H=7168).
  * moe_expert_gate_up_fp8: moe_expert_gate_up with E4M3 operands on the FP8
  * tensor cores; h = silu(g) * u with g = sx*sg[i]*sum(qx*qg) (fp32 accumulate),
- * u likewise; h out in bf16, as for moe_expert_gate_up.  The down projection
- * stays bf16 (moe_expert_down).  hidden % 16 == 0.
+ * u likewise; h out in bf16, as for moe_expert_gate_up.  hidden % 16 == 0.
+ * moe_expert_down_fp8: the down projection with E4M3 operands.  The bf16
+ * intermediate is quantised with moe_quantize_rows_fp8: h_disp [T*k, I] rows
+ * give h8 [T*k, I] + h_scale [T*k]; the shared experts' intermediate
+ * h_shared [T, n_sh*I_sh] gives one row per token, hs8 + hs_scale [T].
+ * Routed down weights qd [S, H, I] codes with one scale per output row
+ * sd [S*H] (quantise w_down viewed as [S*H, I]).  The shared experts' outputs
+ * are summed, so their down weights form one matrix [H, n_sh*I_sh] (expert
+ * j's [H, I_sh] in columns j*I_sh...) quantised per row: qsd [H, n_sh*I_sh],
+ * ssd [H].  y_disp[row, o] = bf16(h_scale[row] * sd[slot*H+o] * sum_i
+ * h8*qd); y_shared[t, o] = hs_scale[t] * ssd[o] * sum_i hs8*qsd in fp32.
+ * inter % 16 == 0 and n_sh*I_sh % 16 == 0.
  * moe_forward_fp8: route (bf16 router), moe_dispatch_fp8,
- * moe_expert_gate_up_fp8, moe_expert_down, moe_combine, intermediates in a
- * workspace of moe_workspace_size_fp8() bytes. */
+ * moe_expert_gate_up_fp8, the two intermediate quantisations,
+ * moe_expert_down_fp8, moe_combine, intermediates in a workspace of
+ * moe_workspace_size_fp8() bytes.  Every expert matrix is E4M3. */
 MOE_API int moe_quantize_rows_fp8(int rows, int cols, const void* x, uint8_t* codes, float* scale, void* stream);
 MOE_API int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
                              const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
@@ -317,11 +328,16 @@ MOE_API int moe_expert_gate_up_fp8(const moe_shape_t* shape, int T, const uint8_
                                    const uint8_t* qg, const float* sg, const uint8_t* qu, const float* su,
                                    const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
                                    void* h_disp, void* h_shared, int mode, void* stream);
+MOE_API int moe_expert_down_fp8(const moe_shape_t* shape, int T, const uint8_t* h8, const float* h_scale,
+                                const uint8_t* hs8, const float* hs_scale, const int32_t* offsets, const uint8_t* qd,
+                                const float* sd, const uint8_t* qsd, const float* ssd, void* y_disp, float* y_shared,
+                                int mode, void* stream);
 MOE_API size_t moe_workspace_size_fp8(const moe_shape_t* shape, int T);
 MOE_API int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
                             const int32_t* replica_of, const uint8_t* qg, const float* sg, const uint8_t* qu,
-                            const float* su, const void* w_down, const uint8_t* qsg, const float* ssg,
-                            const uint8_t* qsu, const float* ssu, const void* ws_down, void* out,
+                            const float* su, const uint8_t* qd, const float* sd, const uint8_t* qsg,
+                            const float* ssg, const uint8_t* qsu, const float* ssu, const uint8_t* qsd,
+                            const float* ssd, void* out,
                             int32_t* topk_idx_out, float* topk_w_out, int32_t* counts_out, int32_t* block_counts_out,
                             int mode, void* ws, size_t ws_bytes, void* stream);
 

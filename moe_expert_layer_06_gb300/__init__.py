@@ -38,7 +38,7 @@ EXPORTS = (
     "moe_workspace_size", "moe_forward", "moe_expert_ffn_noalloc", "moe_route_grouped",
     "moe_eplb_window_bytes", "moe_eplb_window_reset", "moe_eplb_window_push", "moe_eplb_stable_table",
     "moe_eplb_copy_replicas", "moe_quantize_rows_fp8", "moe_dispatch_fp8", "moe_expert_gate_up_fp8",
-    "moe_workspace_size_fp8", "moe_forward_fp8",
+    "moe_workspace_size_fp8", "moe_forward_fp8", "moe_expert_down_fp8",
 )
 
 # capacity of the fixed scratch of moe_expert_ffn_noalloc (include/moe.h)
@@ -94,7 +94,8 @@ _SIG = {
     "moe_dispatch_fp8": (_I, [_P, _I] + [_P] * 13 + [_P]),
     "moe_expert_gate_up_fp8": (_I, [_P, _I] + [_P] * 15 + [_I, _P]),
     "moe_workspace_size_fp8": (_Z, [_P, _I]),
-    "moe_forward_fp8": (_I, [_P, _I] + [_P] * 19 + [_I, _P, _Z, _P]),
+    "moe_expert_down_fp8": (_I, [_P, _I] + [_P] * 11 + [_I, _P]),
+    "moe_forward_fp8": (_I, [_P, _I] + [_P] * 21 + [_I, _P, _Z, _P]),
     "moe_workspace_size": (_Z, [_P, _I]),
     "moe_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
 }
@@ -323,16 +324,23 @@ def moe_expert_gate_up_fp8(shape, T, x8, x_scale, x_disp8, x_disp_scale, offsets
                                         mode, _stream(stream)))
 
 
+def moe_expert_down_fp8(shape, T, h8, h_scale, hs8, hs_scale, offsets, qd, sd, qsd, ssd, y_disp, y_shared,
+                        mode=MOE_FFN_AUTO, stream=None):
+    _check(lib().moe_expert_down_fp8(_shape(shape), T, _ptr(h8), _ptr(h_scale), _ptr(hs8), _ptr(hs_scale),
+                                     _ptr(offsets), _ptr(qd), _ptr(sd), _ptr(qsd), _ptr(ssd), _ptr(y_disp),
+                                     _ptr(y_shared), mode, _stream(stream)))
+
+
 def moe_workspace_size_fp8(shape, T: int) -> int:
     return lib().moe_workspace_size_fp8(_shape(shape), T)
 
 
-def moe_forward_fp8(shape, T, x, w_router, bias, replica_of, qg, sg, qu, su, w_down, qsg, ssg, qsu, ssu, ws_down,
+def moe_forward_fp8(shape, T, x, w_router, bias, replica_of, qg, sg, qu, su, qd, sd, qsg, ssg, qsu, ssu, qsd, ssd,
                     out, topk_idx_out=None, topk_w_out=None, counts_out=None, block_counts_out=None,
                     mode=MOE_FFN_AUTO, ws=None, stream=None):
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(lib().moe_forward_fp8(_shape(shape), T, _ptr(x), _ptr(w_router), _ptr(bias), _ptr(replica_of),
-                                 _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(w_down), _ptr(qsg), _ptr(ssg),
-                                 _ptr(qsu), _ptr(ssu), _ptr(ws_down), _ptr(out), _ptr(topk_idx_out),
+                                 _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(qd), _ptr(sd), _ptr(qsg), _ptr(ssg),
+                                 _ptr(qsu), _ptr(ssu), _ptr(qsd), _ptr(ssd), _ptr(out), _ptr(topk_idx_out),
                                  _ptr(topk_w_out), _ptr(counts_out), _ptr(block_counts_out), mode, _ptr(ws),
                                  ws_bytes, _stream(stream)))

@@ -47,11 +47,13 @@ struct Item {
 // token-chunk byte.
 template <int MODE>
 struct Traits {
-    static constexpr int NA = (MODE == kRouter) ? 1 : 2;
-    static constexpr int kRowsPerItem = (MODE == kDown) ? 256 : 128;
+    static constexpr bool kF8 = (MODE == kGateUpF8 || MODE == kDownF8);  // E4M3 operands
+    static constexpr bool kDownLike = (MODE == kDown || MODE == kDownF8);
     static constexpr bool kGateUpLike = (MODE == kGateUp || MODE == kGateUpF8);
+    static constexpr int NA = (MODE == kRouter) ? 1 : 2;
+    static constexpr int kRowsPerItem = kDownLike ? 256 : 128;
     // elements of K per 128-byte smem row (one pipeline chunk)
-    static constexpr int kChunkK = (MODE == kGateUpF8) ? 128 : 64;
+    static constexpr int kChunkK = kF8 ? 128 : 64;
 };
 
 __host__ __device__ constexpr int pow2_at_least(int v) {
@@ -272,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     tma_load_3d(smem_u32(sa), ma0, fb, ka, it.m0, za, pol_w);
                     if (Traits<MODE>::kGateUpLike)
                         tma_load_3d(smem_u32(sa + kABytes), ma1, fb, ka, it.m0, za, pol_w);
-                    if (MODE == kDown) tma_load_3d(smem_u32(sa + kABytes), ma0, fb, ka, it.m0 + 128, za, pol_w);
+                    if (Traits<MODE>::kDownLike)
+                        tma_load_3d(smem_u32(sa + kABytes), ma0, fb, ka, it.m0 + 128, za, pol_w);
                     for (int bit = 3, off = 0; bit >= 0; --bit) {
                         if (nb & (1 << bit)) {
                             tma_load_3d(smem_u32(sb + off * 2048), mb + bit, fb, kb, bmid, it.row0 + off * 16, pol_x);
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
                 const int nb = (it.nrows + 15) >> 4;
                 const uint32_t idesc =
-                    MODE == kGateUpF8 ? umma_idesc_e4m3(128, nb * 16) : umma_idesc_bf16(128, nb * 16);
+                    Traits<MODE>::kF8 ? umma_idesc_e4m3(128, nb * 16) : umma_idesc_bf16(128, nb * 16);
                 if (*abort_flag || !mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, limit)) {
                     ok = false;
                     break;
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (kc > it.kc0 || kk > 0) ? 1u : 0u;
                         // 32 bytes of K per instruction: 16 bf16 or 32 e4m3 elements
-                        if (MODE == kGateUpF8) {
+                        if (Traits<MODE>::kF8) {
                             umma_e4m3(d0, adesc0 + 2 * kk, bdesc + 2 * kk, idesc, accum);
                             umma_e4m3(d0 + BN, adesc1 + 2 * kk, bdesc + 2 * kk, idesc, accum);
                         } else {
@@ -414,11 +417,31 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         }
                     }
                 } else {
+                    // FP8 down: the token-row scales of this column group
+                    float sxv[16];
+                    if (MODE == kDownF8) {
+                        const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = g * 16 + j;
+                            sxv[j] = col < it.nrows ? __ldg(sbp + col) : 0.0f;
+                        }
+                    }
                     // NA consecutive 128-row output blocks (down: rows m0.. and m0+128..)
 #pragma unroll
                     for (int hh = 0; hh < NA; ++hh) {
                         const int row = mrow + hh * 128;
                         if (row >= mlim) continue;
+                        if (MODE == kDownF8) {
+                            // dequantise: weight-row scale x intermediate-row scale
+                            const float sw = it.shared ? __ldg(a.sa0_scale + row)
+                                                       : __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                if (hh) v1[j] *= sw * sxv[j];
+                                else v0[j] *= sw * sxv[j];
+                            }
+                        }
                         if (MODE == kRouter) {
                             float* dst = reinterpret_cast<float*>(a.out) + (size_t)it.ks * a.T * a.out_ld + row;
 #pragma unroll
@@ -493,6 +516,7 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, c
             case kGateUpF8: return launch_one<kGateUpF8, 32, 5>(args, grid, stream);
             case kGateUp: return launch_one<kGateUp, 32, 5>(args, grid, stream);
             case kDown: return launch_one<kDown, 32, 5>(args, grid, stream);
+            case kDownF8: return launch_one<kDownF8, 32, 5>(args, grid, stream);
             case kRouter: return launch_one<kRouter, 32, 8>(args, grid, stream);
         }
     } else if (bn == kPrefillBN) {
@@ -500,6 +524,7 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, c
             case kGateUpF8: return launch_one<kGateUpF8, kPrefillBN, 4>(args, grid, stream);
             case kGateUp: return launch_one<kGateUp, kPrefillBN, 4>(args, grid, stream);
             case kDown: return launch_one<kDown, kPrefillBN, 4>(args, grid, stream);
+            case kDownF8: return launch_one<kDownF8, kPrefillBN, 4>(args, grid, stream);
             case kRouter: return launch_one<kRouter, kPrefillBN, 5>(args, grid, stream);
         }
     }

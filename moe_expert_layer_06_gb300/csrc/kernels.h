@@ -13,10 +13,12 @@
 namespace moe {
 
 // ---------------------------------------------------------------- grouped swap-AB GEMM (tcgen05)
-// kGateUpF8: gate/up with E4M3 weights and tokens (128-element K chunks,
-// tcgen05 kind::f8f6f4), per-row weight scales and per-token scales applied
-// in the epilogue (they factor out of the K sum).
-enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2, kGateUpF8 = 3 };
+// kGateUpF8 / kDownF8: gate/up and down with E4M3 operands (128-element K
+// chunks, tcgen05 kind::f8f6f4), per-row weight scales and per-row token
+// (or intermediate) scales applied in the epilogue (they factor out of the K
+// sum).  The FP8 shared down is one matrix [H, n_sh*I_sh] on the concatenated
+// shared intermediate.
+enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2, kGateUpF8 = 3, kDownF8 = 4 };
 
 // One launch computes D = A * B^T for a list of work items.  A is a weight
 // tile of 128 output rows (the UMMA M operand), B is a chunk of up to BN
@@ -47,13 +49,13 @@ struct GemmArgs {
     void* out_sh;     // h_sh bf16 [T, n_sh*I_sh] | y_sh f32 [T,H]
     int out_sh_ld;
     int sh_col_stride;  // gate/up: I_sh (column offset of shared expert j in h_sh)
-    // FP8 gate/up only: dequantisation scales
-    const float* a0_scale;  // routed gate rows [S*I]
+    // FP8 modes only: dequantisation scales
+    const float* a0_scale;  // routed gate rows [S*I] | routed down rows [S*H]
     const float* a1_scale;  // routed up rows [S*I]
-    const float* sa0_scale; // shared gate rows [n_sh*I_sh]
+    const float* sa0_scale; // shared gate rows [n_sh*I_sh] | shared down rows [H]
     const float* sa1_scale; // shared up rows [n_sh*I_sh]
-    const float* b_scale;   // dispatched token rows [T*k]
-    const float* sb_scale;  // tokens [T]
+    const float* b_scale;   // dispatched token rows [T*k] | intermediate rows [T*k]
+    const float* sb_scale;  // tokens [T] | shared intermediate rows [T]
     DevStatus st;
 };
 

@@ -462,6 +462,67 @@ static int down_impl(const moe_shape_t* s, int T, const void* h_disp, const void
     return MOE_OK;
 }
 
+static int down_fp8_impl(const moe_shape_t* s, int T, const void* h8, const float* h_scale, const void* hs8,
+                         const float* hs_scale, const int32_t* offsets, const void* qd, const float* sd,
+                         const void* qsd, const float* ssd, void* y_disp, float* y_shared, int mode,
+                         cudaStream_t stream) {
+    const int n_sh = s->n_shared;
+    const int Ks = n_sh * s->inter_shared;  // K of the concatenated shared down matrix
+    if (s->inter % 16 || Ks % 16)
+        return fail(MOE_ERR_INVALID_ARG, "FP8 down needs inter %% 16 == 0 and n_shared*inter_shared %% 16 == 0");
+    NEED(h8, "h8");
+    NEED4(h_scale, "h_scale");
+    NEED4(offsets, "offsets");
+    NEED(qd, "qd");
+    NEED4(sd, "sd");
+    NEED(y_disp, "y_disp");
+    if (n_sh > 0) {
+        NEED(hs8, "hs8");
+        NEED4(hs_scale, "hs_scale");
+        NEED(qsd, "qsd");
+        NEED4(ssd, "ssd");
+        NEED4(y_shared, "y_shared");
+    }
+    DevStatus st;
+    int rc = device_status(&st);
+    if (rc) return rc;
+    const int n = T * s->top_k;
+    const int bn = ffn_bn(T, mode);
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    if ((rc = tmap_weights_f8(&g.a0, qd, s->n_slots, s->hidden, s->inter))) return rc;
+    if ((rc = tmap_rows_f8(g.b, h8, n, s->inter))) return rc;
+    g.a1 = g.a0;
+    if (n_sh > 0) {
+        if ((rc = tmap_weights_f8(&g.sa0, qsd, 1, s->hidden, Ks))) return rc;
+        if ((rc = tmap_rows_f8(g.sb, hs8, T, Ks))) return rc;
+    } else {
+        g.sa0 = g.a0;
+        for (int j = 0; j < 4; ++j) g.sb[j] = g.b[j];
+    }
+    g.sa1 = g.sa0;
+    g.offsets = offsets;
+    g.n_slots = s->n_slots;
+    g.T = T;
+    g.m_routed = s->hidden;
+    g.kc_routed = (s->inter + 127) / 128;
+    g.n_shared = n_sh;
+    g.m_shared = s->hidden;
+    g.kc_shared = (Ks + 127) / 128;
+    g.kc_per_sh = 1;
+    g.out = y_disp;
+    g.out_ld = s->hidden;
+    g.out_sh = y_shared;
+    g.out_sh_ld = s->hidden;
+    g.a0_scale = sd;
+    g.sa0_scale = ssd;
+    g.b_scale = h_scale;
+    g.sb_scale = hs_scale;
+    g.st = st;
+    MOE_CUDA(launch_gemm(kDownF8, bn, g, num_sms(), stream), "FP8 down gemm launch");
+    return MOE_OK;
+}
+
 static size_t ffn_ws(const moe_shape_t* s, int T) {
     const size_t n = (size_t)T * s->top_k;
     return align256(n * s->inter * 2) + align256((size_t)T * s->n_shared * s->inter_shared * 2);
@@ -501,7 +562,7 @@ static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
 // FP8 forward: the bf16 layout plus the quantised tokens and their dispatched copies
 struct FwdLayoutF8 {
     FwdLayout base;
-    size_t x8, x_scale, x_disp8, x_disp_scale, total;
+    size_t x8, x_scale, x_disp8, x_disp_scale, h8, h_scale, hs8, hs_scale, total;
 };
 
 static FwdLayoutF8 fwd_layout_f8(const moe_shape_t* s, int T) {
@@ -518,6 +579,10 @@ static FwdLayoutF8 fwd_layout_f8(const moe_shape_t* s, int T) {
     L.x_scale = take((size_t)T * 4);
     L.x_disp8 = take(n * s->hidden);
     L.x_disp_scale = take(n * 4);
+    L.h8 = take(n * s->inter);
+    L.h_scale = take(n * 4);
+    L.hs8 = take((size_t)T * s->n_shared * s->inter_shared);
+    L.hs_scale = take((size_t)T * 4);
     L.total = off;
     return L;
 }
@@ -877,6 +942,18 @@ int moe_expert_gate_up_fp8(const moe_shape_t* shape, int T, const uint8_t* x8, c
                             ssu, h_disp, h_shared, mode, as_stream(stream));
 }
 
+int moe_expert_down_fp8(const moe_shape_t* shape, int T, const uint8_t* h8, const float* h_scale, const uint8_t* hs8,
+                        const float* hs_scale, const int32_t* offsets, const uint8_t* qd, const float* sd,
+                        const uint8_t* qsd, const float* ssd, void* y_disp, float* y_shared, int mode,
+                        void* stream) {
+    int rc = check_shape(shape, T);
+    if (rc) return rc;
+    if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
+    if (T == 0) return MOE_OK;
+    return down_fp8_impl(shape, T, h8, h_scale, hs8, hs_scale, offsets, qd, sd, qsd, ssd, y_disp, y_shared, mode,
+                         as_stream(stream));
+}
+
 size_t moe_workspace_size_fp8(const moe_shape_t* shape, int T) {
     if (check_shape(shape, T)) return 0;
     return fwd_layout_f8(shape, T).total;
@@ -884,14 +961,17 @@ size_t moe_workspace_size_fp8(const moe_shape_t* shape, int T) {
 
 int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
                     const int32_t* replica_of, const uint8_t* qg, const float* sg, const uint8_t* qu,
-                    const float* su, const void* w_down, const uint8_t* qsg, const float* ssg, const uint8_t* qsu,
-                    const float* ssu, const void* ws_down, void* out, int32_t* topk_idx_out, float* topk_w_out,
+                    const float* su, const uint8_t* qd, const float* sd, const uint8_t* qsg, const float* ssg,
+                    const uint8_t* qsu, const float* ssu, const uint8_t* qsd, const float* ssd, void* out,
+                    int32_t* topk_idx_out, float* topk_w_out,
                     int32_t* counts_out, int32_t* block_counts_out, int mode, void* ws, size_t ws_bytes,
                     void* stream) {
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
-    if (shape->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
+    if (shape->hidden % 16 || shape->inter % 16 || (shape->n_shared * shape->inter_shared) % 16)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "FP8 rows need hidden, inter and n_shared*inter_shared to be multiples of 16");
     if (T == 0) return MOE_OK;
     NEED(out, "out");
     const FwdLayoutF8 L = fwd_layout_f8(shape, T);
@@ -920,7 +1000,19 @@ int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* 
                                      reinterpret_cast<float*>(b + L.x_disp_scale), offsets, qg, sg, qu, su, qsg, ssg,
                                      qsu, ssu, h, hs, mode, stream)))
         return rc;
-    if ((rc = moe_expert_down(shape, T, h, hs, offsets, w_down, ws_down, b + B.y_disp, y_sh, mode, stream)))
+    // the bf16 intermediates as E4M3 rows: one per (token, routed expert), one per token for the shared experts
+    const int n = T * shape->top_k;
+    const int Ks = shape->n_shared * shape->inter_shared;
+    cudaStream_t st = as_stream(stream);
+    float* h_scale = reinterpret_cast<float*>(b + L.h_scale);
+    float* hs_scale = Ks > 0 ? reinterpret_cast<float*>(b + L.hs_scale) : nullptr;
+    MOE_CUDA(launch_quantize_rows(reinterpret_cast<const uint16_t*>(h), n, shape->inter, b + L.h8, h_scale, st),
+             "intermediate quantize launch");
+    if (Ks > 0)
+        MOE_CUDA(launch_quantize_rows(reinterpret_cast<const uint16_t*>(hs), T, Ks, b + L.hs8, hs_scale, st),
+                 "shared intermediate quantize launch");
+    if ((rc = moe_expert_down_fp8(shape, T, b + L.h8, h_scale, Ks > 0 ? b + L.hs8 : nullptr, hs_scale, offsets, qd,
+                                  sd, qsd, ssd, b + B.y_disp, y_sh, mode, stream)))
         return rc;
     return moe_combine(shape, T, b + B.y_disp, inv, tw, y_sh, out, stream);
 }

@@ -37,6 +37,26 @@ def test_library_exports_every_declared_symbol():
     assert m.lib().moe_abi_version() == 1
 
 
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature has as many arguments as the declaration, and
+    integer parameters sit where the header has int / size_t / double."""
+    src = open(HEADER).read()
+    decls = re.findall(r"^MOE_API [^(]*?\b(moe_\w+)\(([^;]*?)\);", src, flags=re.M | re.S)
+    assert len(decls) == len(m.EXPORTS)
+    kinds = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "double": ctypes.c_double, "uint64_t": ctypes.c_uint64}
+    for name, params in decls:
+        params = " ".join(params.split())
+        plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        sig = m._SIG[name][1]
+        assert len(sig) == len(plist), (name, len(sig), len(plist))
+        for p, t in zip(plist, sig):
+            if "*" in p:
+                assert t is ctypes.c_void_p, (name, p)
+            else:
+                base = p.rsplit(" ", 1)[0].replace("const ", "").strip()
+                assert t is kinds[base], (name, p)
+
+
 def _shape(**kw):
     return m.Shape.of(mi.WORKLOADS["decode_t32"].with_(**kw))
 

@@ -1,8 +1,10 @@
 """FP8 path on the GPU against the fp64 oracle of the same quantised layer.
 
-Quantisation decides integers (codes), so codes and scales must match the
-oracle bit-exactly; the FP8 GEMM then sees exactly the oracle's operands and
-its output is held to the same tolerance as the bf16 path.
+Quantisation decides integers (codes), so codes and scales of the same bf16
+input must match the oracle bit-exactly; each FP8 GEMM then sees exactly the
+oracle's operands and its output is held to the same tolerance as the bf16
+path.  The layer test compares with the oracle's whole FP8 layer, whose
+intermediate h is its own (fp64, then bf16) rather than the kernel's.
 """
 import numpy as np
 import pytest
@@ -17,7 +19,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 # ragged in every GEMM dimension; hidden a multiple of 16 for 1-byte rows
-MID8 = mi.WORKLOADS["tiny"].with_(name="mid8", tokens=100, hidden=608, inter=328, n_experts=16, top_k=4,
+MID8 = mi.WORKLOADS["tiny"].with_(name="mid8", tokens=100, hidden=608, inter=336, n_experts=16, top_k=4,
                                   n_shared=2, inter_shared=200, n_slots=16, n_blocks=4)
 REP8 = mi.WORKLOADS["tiny"].with_(name="rep8", tokens=64, hidden=128, inter=64, n_experts=8, top_k=2,
                                   n_shared=1, inter_shared=64, n_slots=12, n_blocks=4)
@@ -48,14 +50,71 @@ def test_row_quantizer_is_bit_exact():
 def _quantised_weights(w, rep=None):
     wg, wu, wd = mi.stacked_expert_weights(w, rep)
     sg, su, sd = mi.stacked_shared_weights(w)
-    H = w.hidden
-    q = {}
-    q["qg"], q["sg"] = oracle.quantize_rows_e4m3(wg.reshape(-1, H))
-    q["qu"], q["su"] = oracle.quantize_rows_e4m3(wu.reshape(-1, H))
-    q["qsg"], q["ssg"] = oracle.quantize_rows_e4m3(sg.reshape(-1, H))
-    q["qsu"], q["ssu"] = oracle.quantize_rows_e4m3(su.reshape(-1, H))
-    q["wd"] = wd
-    return q, sd
+    return oracle.quantize_layer_fp8(w, wg, wu, wd, sg, su, sd)
+
+
+def _dev(q):
+    return {k_: (_u8(v) if k_.startswith("q") else _f32(v)) for k_, v in q.items()}
+
+
+def test_shared_down_matrix_quantised_on_the_device_is_bit_exact():
+    w = MID8
+    _, _, sd = mi.stacked_shared_weights(w)
+    mat = oracle.shared_down_matrix(sd)
+    c_o, s_o = oracle.quantize_rows_e4m3(mat)
+    codes = torch.empty(mat.shape, dtype=torch.uint8, device=DEV)
+    scale = torch.empty(mat.shape[0], dtype=torch.float32, device=DEV)
+    m.moe_quantize_rows_fp8(sd.to(DEV).permute(1, 0, 2).reshape(w.hidden, -1).contiguous(), codes, scale)
+    assert np.array_equal(codes.cpu().numpy(), c_o) and np.array_equal(scale.cpu().numpy(), s_o)
+
+
+@pytest.mark.parametrize("mode", [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL])
+@pytest.mark.parametrize("name", ["tiny", "mid8"])
+def test_fp8_intermediate_and_down_stage(name, mode):
+    """Gate/up on the GPU, then the stage under test on the GPU's own h: the
+    row quantiser (bit-exact against the oracle on the same bf16 h) and the
+    FP8 down GEMM (against the oracle's down row on the same codes)."""
+    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8}[name]
+    T, k, S, H, I = w.tokens, w.top_k, w.n_slots, w.hidden, w.inter
+    Ks = w.n_shared * w.inter_shared
+    q = _quantised_weights(w)
+    d = _dev(q)
+    idx, _ = oracle.topk_softmax(mi.fp32_logits(w).double(), k)
+    x = mi.hidden_states(w)
+    n = T * k
+    i32 = dict(dtype=torch.int32, device=DEV)
+    so, c, b = torch.empty(n, **i32), torch.empty(S + 1, **i32), torch.empty(w.n_blocks, **i32)
+    off, perm, inv = torch.empty(S + 2, **i32), torch.empty(n, **i32), torch.empty(n, **i32)
+    x8 = torch.empty((T, H), dtype=torch.uint8, device=DEV)
+    xs = torch.empty(T, dtype=torch.float32, device=DEV)
+    xd8 = torch.empty((n, H), dtype=torch.uint8, device=DEV)
+    xds = torch.empty(n, dtype=torch.float32, device=DEV)
+    m.moe_dispatch_fp8(w, T, x.to(DEV), torch.from_numpy(idx).to(DEV), None, so, c, b, off, perm, inv, x8, xs, xd8,
+                       xds)
+    h = torch.empty((n, I), dtype=torch.bfloat16, device=DEV)
+    hs = torch.empty((T, Ks), dtype=torch.bfloat16, device=DEV)
+    m.moe_expert_gate_up_fp8(w, T, x8, xs, xd8, xds, off, d["qg"], d["sg"], d["qu"], d["su"], d["qsg"], d["ssg"],
+                             d["qsu"], d["ssu"], h, hs, mode=mode)
+    h8, h8s = torch.empty((n, I), dtype=torch.uint8, device=DEV), torch.empty(n, dtype=torch.float32, device=DEV)
+    hs8, hs8s = torch.empty((T, Ks), dtype=torch.uint8, device=DEV), torch.empty(T, dtype=torch.float32, device=DEV)
+    m.moe_quantize_rows_fp8(h, h8, h8s)
+    m.moe_quantize_rows_fp8(hs, hs8, hs8s)
+    y = torch.empty((n, H), dtype=torch.bfloat16, device=DEV)
+    ysh = torch.empty((T, H), dtype=torch.float32, device=DEV)
+    m.moe_expert_down_fp8(w, T, h8, h8s, hs8, hs8s, off, d["qd"], d["sd"], d["qsd"], d["ssd"], y, ysh, mode=mode)
+    assert m.moe_check_status() == 0, m.last_error()
+    qh_o, sh_o = oracle.quantize_rows_e4m3(h.cpu())
+    assert np.array_equal(h8.cpu().numpy(), qh_o) and np.array_equal(h8s.cpu().numpy(), sh_o)
+    qhs_o, shs_o = oracle.quantize_rows_e4m3(hs.cpu())
+    assert np.array_equal(hs8.cpu().numpy(), qhs_o) and np.array_equal(hs8s.cpu().numpy(), shs_o)
+    offs = off.cpu().numpy()
+    slot_of_row = np.searchsorted(offs[:S + 1], np.arange(n), side="right") - 1
+    qd = q["qd"].reshape(S, H, I)
+    sd = q["sd"].reshape(S, H)
+    y_o = np.stack([oracle.down_row_fp8(qh_o[r], sh_o[r], qd[s_], sd[s_]) for r, s_ in enumerate(slot_of_row)])
+    assert_close(to_np(y), y_o, what=f"{name} FP8 down (routed)")
+    ysh_o = np.stack([oracle.down_row_fp8(qhs_o[t], shs_o[t], q["qsd"], q["ssd"]) for t in range(T)])
+    assert_close(ysh.cpu().numpy().astype(np.float64), ysh_o, what=f"{name} FP8 down (shared)")
 
 
 @pytest.mark.parametrize("name", ["tiny", "mid8", "rep8"])
@@ -97,16 +156,17 @@ def test_fp8_layer_matches_fp8_oracle(name, mode):
         rep = oracle.plan_replicas(w, np.arange(w.n_experts)[::-1].copy(), w.n_slots - w.n_experts)
     T, H = w.tokens, w.hidden
     x, wr = mi.hidden_states(w), mi.router_weight(w)
-    q, sd = _quantised_weights(w, rep)
-    ref = oracle.moe_forward_fp8(w, x, wr, None, rep, q, sd)
+    q = _quantised_weights(w, rep)
+    ref = oracle.moe_forward_fp8(w, x, wr, None, rep, q)
     lo = oracle.router_logits(w, x, wr, None)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     idx = torch.empty((T, w.top_k), dtype=torch.int32, device=DEV)
     ws = torch.empty(m.moe_workspace_size_fp8(w, T), dtype=torch.uint8, device=DEV)
     repd = torch.from_numpy(rep).to(DEV) if rep is not None else None
-    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), None, repd, _u8(q["qg"]), _f32(q["sg"]), _u8(q["qu"]),
-                      _f32(q["su"]), q["wd"].to(DEV), _u8(q["qsg"]), _f32(q["ssg"]), _u8(q["qsu"]), _f32(q["ssu"]),
-                      sd.to(DEV), out, topk_idx_out=idx, mode=mode, ws=ws)
+    d = _dev(q)
+    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), None, repd, d["qg"], d["sg"], d["qu"], d["su"], d["qd"], d["sd"],
+                      d["qsg"], d["ssg"], d["qsu"], d["ssu"], d["qsd"], d["ssd"], out, topk_idx_out=idx, mode=mode,
+                      ws=ws)
     assert m.moe_check_status() == 0, m.last_error()
     sure = check_topk(idx.cpu().numpy(), ref["idx"], lo, w.top_k)
     assert_close(to_np(out)[sure], ref["out"][sure], what=f"{name} fp8 layer")
@@ -118,29 +178,27 @@ _EXPERTS = {}
 def test_fp8_layer_full_decode_shape_sampled_tokens():
     w = mi.WORKLOADS["decode_t32"]
     T, H, k = w.tokens, w.hidden, w.top_k
+
+    def quant(t):
+        q = torch.empty(t.shape, dtype=torch.uint8, device=DEV)
+        sc = torch.empty(t.numel() // t.shape[-1], dtype=torch.float32, device=DEV)
+        m.moe_quantize_rows_fp8(t.view(-1, t.shape[-1]), q, sc)
+        return q, sc
+
     wg, wu, wd = mi.stacked_expert_weights(w, device=DEV)
+    (qg, s_g), (qu, s_u), (qd, s_d) = quant(wg), quant(wu), quant(wd)
+    del wg, wu, wd
     sg, su, sd = mi.stacked_shared_weights(w, device=DEV)
-    qg = torch.empty(wg.shape, dtype=torch.uint8, device=DEV)
-    qu = torch.empty(wu.shape, dtype=torch.uint8, device=DEV)
-    s_g = torch.empty(wg.shape[0] * wg.shape[1], dtype=torch.float32, device=DEV)
-    s_u = torch.empty_like(s_g)
-    m.moe_quantize_rows_fp8(wg.view(-1, H), qg, s_g)
-    m.moe_quantize_rows_fp8(wu.view(-1, H), qu, s_u)
-    del wg, wu
-    qsg = torch.empty(sg.shape, dtype=torch.uint8, device=DEV)
-    qsu = torch.empty(su.shape, dtype=torch.uint8, device=DEV)
-    s_sg = torch.empty(sg.shape[0] * sg.shape[1], dtype=torch.float32, device=DEV)
-    s_su = torch.empty_like(s_sg)
-    m.moe_quantize_rows_fp8(sg.view(-1, H), qsg, s_sg)
-    m.moe_quantize_rows_fp8(su.view(-1, H), qsu, s_su)
+    (qsg, s_sg), (qsu, s_su) = quant(sg), quant(su)
+    qsd, s_sd = quant(sd.permute(1, 0, 2).reshape(H, -1).contiguous())
     x = mi.hidden_states(w)
     wr = mi.router_weight(w)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
     tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
     ws = torch.empty(m.moe_workspace_size_fp8(w, T), dtype=torch.uint8, device=DEV)
-    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), None, None, qg, s_g, qu, s_u, wd, qsg, s_sg, qsu, s_su, sd, out,
-                      topk_idx_out=idx, topk_w_out=tw, ws=ws)
+    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), None, None, qg, s_g, qu, s_u, qd, s_d, qsg, s_sg, qsu, s_su, qsd,
+                      s_sd, out, topk_idx_out=idx, topk_w_out=tw, ws=ws)
     assert m.moe_check_status() == 0, m.last_error()
     lo = parallel_router_logits(w, x, wr, None)
     idx_o, wt_o = oracle.topk_softmax(lo, k)
@@ -148,17 +206,19 @@ def test_fp8_layer_full_decode_shape_sampled_tokens():
     toks = [t for t in (0, 13, 31) if sure[t]]
     qx, sx = oracle.quantize_rows_e4m3(x)
     sgc, suc, sdc = mi.stacked_shared_weights(w)
-    shq = [oracle.quantize_rows_e4m3(sgc[j]) + oracle.quantize_rows_e4m3(suc[j]) for j in range(w.n_shared)]
+    qsh = {}
+    qsh["qsg"], qsh["ssg"] = oracle.quantize_rows_e4m3(sgc.reshape(-1, H))
+    qsh["qsu"], qsh["ssu"] = oracle.quantize_rows_e4m3(suc.reshape(-1, H))
+    qsh["qsd"], qsh["ssd"] = oracle.quantize_rows_e4m3(oracle.shared_down_matrix(sdc))
     for t in toks:
         ys = []
         for e in idx_o[t]:
             if int(e) not in _EXPERTS:
-                g, u, d = mi.expert_weights(w, int(e))
-                _EXPERTS[int(e)] = (oracle.quantize_rows_e4m3(g), oracle.quantize_rows_e4m3(u), d)
-            (cg, scg), (cu, scu), d = _EXPERTS[int(e)]
-            ys.append(oracle.swiglu_row_fp8(qx[t], sx[t], cg, scg, cu, scu, d))
-        ysh = sum(oracle.swiglu_row_fp8(qx[t], sx[t], a, b_, c, d_, sdc[j])
-                  for j, (a, b_, c, d_) in enumerate(shq))
+                g, u, dn = mi.expert_weights(w, int(e))
+                _EXPERTS[int(e)] = tuple(oracle.quantize_rows_e4m3(a) for a in (g, u, dn))
+            (cg, scg), (cu, scu), (cd, scd) = _EXPERTS[int(e)]
+            ys.append(oracle.swiglu_row_fp8(qx[t], sx[t], cg, scg, cu, scu, cd, scd))
+        ysh = oracle.shared_row_fp8(w, qx[t], sx[t], qsh)
         ref = oracle.combine(w.with_(tokens=1), 1, np.stack(ys), np.arange(k, dtype=np.int32), wt_o[t:t + 1],
                              ysh[None, :])
         assert_close(to_np(out)[t:t + 1], ref, what=f"fp8 decode token {t}")
