@@ -37,17 +37,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int row = __ldg(inv_perm + (size_t)t * k + j);
-            const float w = __ldg(topk_w + (size_t)t * k + j);
-            float y[8];
-            unpack8(__ldg(y_disp + (size_t)row * vec_per_row + c), y);
+        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+        if (y_shared) {  // independent of the gathers: issue first
+            s0 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2);
+            s1 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2 + 1);
+        }
+        // up to 8 assignments at a time: all row indices, then all rows, then the sum in ascending j
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            int row[8];
+            float w[8];
+            uint4 yv[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, y[i], acc[i]);
+            for (int u = 0; u < 8; ++u) {
+                if (j0 + u < k) {
+                    row[u] = __ldg(inv_perm + (size_t)t * k + j0 + u);
+                    w[u] = __ldg(topk_w + (size_t)t * k + j0 + u);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (j0 + u < k) yv[u] = __ldg(y_disp + (size_t)row[u] * vec_per_row + c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (j0 + u < k) {
+                    float y[8];
+                    unpack8(yv[u], y);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[u], y[i], acc[i]);
+                }
+            }
         }
         if (y_shared) {
-            const float4 s0 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2);
-            const float4 s1 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2 + 1);
             acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
             acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
         }

@@ -140,18 +140,38 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
     }
 }
 
-// x_disp[row] = x[perm[row] / k], 16-byte vectors, one warp per row.
-__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint4* __restrict__ x,
-                                                           const int32_t* __restrict__ perm, int n_rows,
-                                                           int k, int vec_per_row, uint4* __restrict__ x_disp) {
-    const int lane = threadIdx.x & 31;
-    const int wpb = blockDim.x >> 5;
-    for (int row = blockIdx.x * wpb + (threadIdx.x >> 5); row < n_rows; row += gridDim.x * wpb) {
-        const int t = perm[row] / k;
+// x_disp[row] = x[perm[row] / k] in 16-byte vectors.  A row is spread over
+// tpr threads (a multiple of 32) that each issue all of their (at most
+// kCopyVpt) loads before storing; blockDim.x / tpr rows per CTA.
+constexpr int kCopyVpt = 8;
+constexpr int kCopyThreads = 256;
+
+__global__ void __launch_bounds__(kCopyThreads) scatter_rows_kernel(const uint4* __restrict__ x,
+                                                                    const int32_t* __restrict__ perm, int n_rows,
+                                                                    int k, int vec_per_row, int tpr,
+                                                                    uint4* __restrict__ x_disp) {
+    const int rows_per_cta = blockDim.x / tpr;
+    const int sub = threadIdx.x / tpr;
+    const int t0 = threadIdx.x - sub * tpr;
+    for (int r0 = blockIdx.x * rows_per_cta; r0 < n_rows; r0 += gridDim.x * rows_per_cta) {
+        const int row = r0 + sub;
+        if (row >= n_rows) continue;
+        const int t = __ldg(perm + row) / k;
         const uint4* src = x + (size_t)t * vec_per_row;
         uint4* dst = x_disp + (size_t)row * vec_per_row;
-#pragma unroll 4
-        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+        for (int c0 = 0; c0 < vec_per_row; c0 += kCopyVpt * tpr) {
+            uint4 v[kCopyVpt];
+#pragma unroll
+            for (int j = 0; j < kCopyVpt; ++j) {
+                const int c = c0 + t0 + j * tpr;
+                if (c < vec_per_row) v[j] = __ldg(src + c);
+            }
+#pragma unroll
+            for (int j = 0; j < kCopyVpt; ++j) {
+                const int c = c0 + t0 + j * tpr;
+                if (c < vec_per_row) dst[c] = v[j];
+            }
+        }
     }
 }
 
@@ -179,12 +199,15 @@ cudaError_t launch_index_pass(const DispatchArgs& a, cudaStream_t stream) {
 cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* perm, int n_rows, int k, int hidden,
                                 uint16_t* x_disp, cudaStream_t stream) {
     if (n_rows <= 0) return cudaSuccess;
-    const int wpb = 8;
-    int blocks = (n_rows + wpb - 1) / wpb;
-    const int cap = num_sms() * 16;
+    const int vec = hidden / 8;
+    int tpr = 32;  // the fewest warps that cover the row in one round of loads (at most the CTA)
+    while (tpr * kCopyVpt < vec && tpr < kCopyThreads) tpr <<= 1;
+    const int rows_per_cta = kCopyThreads / tpr;
+    int blocks = (n_rows + rows_per_cta - 1) / rows_per_cta;
+    const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    scatter_rows_kernel<<<blocks, wpb * 32, 0, stream>>>(reinterpret_cast<const uint4*>(x), perm, n_rows, k,
-                                                         hidden / 8, reinterpret_cast<uint4*>(x_disp));
+    scatter_rows_kernel<<<blocks, kCopyThreads, 0, stream>>>(reinterpret_cast<const uint4*>(x), perm, n_rows, k,
+                                                            vec, tpr, reinterpret_cast<uint4*>(x_disp));
     return cudaGetLastError();
 }
 

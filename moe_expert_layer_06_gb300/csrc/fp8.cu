@@ -13,59 +13,136 @@
 namespace moe {
 namespace {
 
-// One warp per row, 8 bf16 (16 bytes) per lane per step.
-__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ x, int rows, int vec_per_row,
-                                                            uint2* __restrict__ codes, float* __restrict__ scale) {
+// E4M3 codes of 8 bf16 values (one 16-byte vector) at scale s, packed into 8 bytes.
+__device__ __forceinline__ uint2 encode8(const uint4 q, float s) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t packed[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __fdiv_rn(__uint_as_float(w[i] << 16), s);
+        const float hi = __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), s);
+        const uint32_t c0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
+        packed[i >> 1] |= (c0 | (c1 << 8)) << ((i & 1) * 16);
+    }
+    return make_uint2(packed[0], packed[1]);
+}
+
+__device__ __forceinline__ float amax8(const uint4 q, float m) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+    return m;
+}
+
+__device__ __forceinline__ float row_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f; }
+
+// Single pass: a row is spread over tpr threads (a multiple of 32), each
+// holding up to kVpt 16-byte vectors in registers: load, amax over the row
+// (warp shuffles, then shared memory across the row's warps), encode from the
+// registers, store.  blockDim.x / tpr rows per CTA, grid-stride over rows.
+constexpr int kVpt = 8;
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const uint4* __restrict__ x, int rows,
+                                                                      int vec_per_row, int tpr,
+                                                                      uint2* __restrict__ codes,
+                                                                      float* __restrict__ scale) {
+    __shared__ float part[kQuantThreads / 32];
+    const int rows_per_cta = blockDim.x / tpr;
+    const int sub = threadIdx.x / tpr;  // row slot of this thread in the CTA
+    const int t = threadIdx.x - sub * tpr;
+    const int lane = threadIdx.x & 31;
+    const int wpr = tpr >> 5;  // warps per row
+    for (int r0 = blockIdx.x * rows_per_cta; r0 < rows; r0 += gridDim.x * rows_per_cta) {
+        const int r = r0 + sub;
+        const bool live = r < rows;
+        const uint4* src = x + (size_t)r * vec_per_row;
+        uint4 v[kVpt];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) {
+            const int c = t + j * tpr;
+            v[j] = make_uint4(0, 0, 0, 0);
+            if (live && c < vec_per_row) v[j] = __ldg(src + c);
+        }
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) amax = amax8(v[j], amax);
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        if (wpr > 1) {
+            __syncthreads();  // part[] free from the previous round
+            if (lane == 0) part[threadIdx.x >> 5] = amax;
+            __syncthreads();
+            const int w0 = sub * wpr;
+            for (int q = 0; q < wpr; ++q) amax = fmaxf(amax, part[w0 + q]);
+        }
+        const float s = row_scale(amax);
+        if (live) {
+            if (t == 0) scale[r] = s;
+            uint2* dst = codes + (size_t)r * vec_per_row;
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                const int c = t + j * tpr;
+                if (c < vec_per_row) dst[c] = encode8(v[j], s);
+            }
+        }
+    }
+}
+
+// Rows too long for the registers of one CTA: one warp per row, two passes.
+__global__ void __launch_bounds__(256) quantize_long_rows_kernel(const uint4* __restrict__ x, int rows,
+                                                                 int vec_per_row, uint2* __restrict__ codes,
+                                                                 float* __restrict__ scale) {
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows; r += gridDim.x * wpb) {
         const uint4* src = x + (size_t)r * vec_per_row;
         float amax = 0.0f;
-        for (int v = lane; v < vec_per_row; v += 32) {
-            const uint4 q = __ldg(src + v);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-                amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
-            }
-        }
+        for (int c = lane; c < vec_per_row; c += 32) amax = amax8(__ldg(src + c), amax);
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-        const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+        const float s = row_scale(amax);
         if (lane == 0) scale[r] = s;
         uint2* dst = codes + (size_t)r * vec_per_row;
-        for (int v = lane; v < vec_per_row; v += 32) {
-            const uint4 q = __ldg(src + v);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-            uint32_t packed[2] = {0, 0};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = __fdiv_rn(__uint_as_float(w[i] << 16), s);
-                const float hi = __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), s);
-                const uint32_t c0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
-                const uint32_t c1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
-                packed[i >> 1] |= (c0 | (c1 << 8)) << ((i & 1) * 16);
-            }
-            dst[v] = make_uint2(packed[0], packed[1]);
-        }
+        for (int c = lane; c < vec_per_row; c += 32) dst[c] = encode8(__ldg(src + c), s);
     }
 }
 
-// x_disp8[row] = x8[perm[row] / k], one warp per row, 16-byte vectors; lane 0 copies the scale.
-__global__ void __launch_bounds__(256) scatter_fp8_kernel(const uint4* __restrict__ x8, const float* __restrict__ xs,
-                                                          const int32_t* __restrict__ perm, int n_rows, int k,
-                                                          int vec_per_row, uint4* __restrict__ out,
-                                                          float* __restrict__ out_scale) {
-    const int lane = threadIdx.x & 31;
-    const int wpb = blockDim.x >> 5;
-    for (int row = blockIdx.x * wpb + (threadIdx.x >> 5); row < n_rows; row += gridDim.x * wpb) {
-        const int t = perm[row] / k;
+// x_disp8[row] = x8[perm[row] / k] (16-byte vectors, a row over tpr threads that
+// issue all of their loads before storing), x_disp_scale[row] likewise.
+__global__ void __launch_bounds__(kQuantThreads) scatter_fp8_kernel(const uint4* __restrict__ x8,
+                                                                    const float* __restrict__ xs,
+                                                                    const int32_t* __restrict__ perm, int n_rows,
+                                                                    int k, int vec_per_row, int tpr,
+                                                                    uint4* __restrict__ out,
+                                                                    float* __restrict__ out_scale) {
+    const int rows_per_cta = blockDim.x / tpr;
+    const int sub = threadIdx.x / tpr;
+    const int t0 = threadIdx.x - sub * tpr;
+    for (int r0 = blockIdx.x * rows_per_cta; r0 < n_rows; r0 += gridDim.x * rows_per_cta) {
+        const int row = r0 + sub;
+        if (row >= n_rows) continue;
+        const int t = __ldg(perm + row) / k;
         const uint4* src = x8 + (size_t)t * vec_per_row;
         uint4* dst = out + (size_t)row * vec_per_row;
-#pragma unroll 4
-        for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
-        if (lane == 0) out_scale[row] = __ldg(xs + t);
+        for (int c0 = 0; c0 < vec_per_row; c0 += kVpt * tpr) {
+            uint4 v[kVpt];
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                const int c = c0 + t0 + j * tpr;
+                if (c < vec_per_row) v[j] = __ldg(src + c);
+            }
+#pragma unroll
+            for (int j = 0; j < kVpt; ++j) {
+                const int c = c0 + t0 + j * tpr;
+                if (c < vec_per_row) dst[c] = v[j];
+            }
+        }
+        if (t0 == 0) out_scale[row] = __ldg(xs + t);
     }
 }
 
@@ -74,25 +151,39 @@ __global__ void __launch_bounds__(256) scatter_fp8_kernel(const uint4* __restric
 cudaError_t launch_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t* codes, float* scale,
                                  cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
-    const int wpb = 8;
-    int blocks = (rows + wpb - 1) / wpb;
-    const int cap = num_sms() * 16;
+    const int vec = cols / 8;
+    const int cap = num_sms() * 8;
+    if (vec > kVpt * kQuantThreads) {
+        int blocks = (rows + 7) / 8;
+        if (blocks > cap) blocks = cap;
+        quantize_long_rows_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), rows, vec,
+                                                              reinterpret_cast<uint2*>(codes), scale);
+        return cudaGetLastError();
+    }
+    // threads per row: the fewest warps whose registers hold the row
+    int tpr = 32;
+    while (tpr * kVpt < vec) tpr <<= 1;
+    const int rows_per_cta = kQuantThreads / tpr;
+    int blocks = (rows + rows_per_cta - 1) / rows_per_cta;
     if (blocks > cap) blocks = cap;
-    quantize_rows_kernel<<<blocks, wpb * 32, 0, stream>>>(reinterpret_cast<const uint4*>(x), rows, cols / 8,
-                                                          reinterpret_cast<uint2*>(codes), scale);
+    quantize_rows_kernel<<<blocks, kQuantThreads, 0, stream>>>(reinterpret_cast<const uint4*>(x), rows, vec, tpr,
+                                                               reinterpret_cast<uint2*>(codes), scale);
     return cudaGetLastError();
 }
 
 cudaError_t launch_scatter_fp8(const uint8_t* x8, const float* x_scale, const int32_t* perm, int n_rows, int k,
                                int row_bytes, uint8_t* x_disp8, float* x_disp_scale, cudaStream_t stream) {
     if (n_rows <= 0) return cudaSuccess;
-    const int wpb = 8;
-    int blocks = (n_rows + wpb - 1) / wpb;
-    const int cap = num_sms() * 16;
+    const int vec = row_bytes / 16;
+    int tpr = 32;
+    while (tpr * kVpt < vec && tpr < kQuantThreads) tpr <<= 1;
+    const int rows_per_cta = kQuantThreads / tpr;
+    int blocks = (n_rows + rows_per_cta - 1) / rows_per_cta;
+    const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    scatter_fp8_kernel<<<blocks, wpb * 32, 0, stream>>>(reinterpret_cast<const uint4*>(x8), x_scale, perm, n_rows, k,
-                                                        row_bytes / 16, reinterpret_cast<uint4*>(x_disp8),
-                                                        x_disp_scale);
+    scatter_fp8_kernel<<<blocks, kQuantThreads, 0, stream>>>(reinterpret_cast<const uint4*>(x8), x_scale, perm,
+                                                             n_rows, k, vec, tpr, reinterpret_cast<uint4*>(x_disp8),
+                                                             x_disp_scale);
     return cudaGetLastError();
 }
 

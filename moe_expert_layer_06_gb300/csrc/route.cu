@@ -17,28 +17,32 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 }
 
 // tpc (1..8) tokens per CTA, grid-stride: all threads sum the K-split partials
-// of the CTA's tokens (coalesced over experts, eight loads in flight, added in
-// split order) into shared memory, then warp w runs the softmax and the k
-// arg-max rounds of token w.  Few tokens (decode) use one token per CTA so
-// that enough CTAs share the partial sums.
+// of the CTA's tokens (coalesced over experts, eight loads in flight) into
+// shared memory, then warp w runs the softmax and the k arg-max rounds of
+// token w.  Few tokens (decode) use one token per CTA of 1024 threads: each
+// logit's partials are summed by kGroups threads (group g takes splits g,
+// g + kGroups, ... in order) and the group sums added in group order, so the
+// result does not depend on scheduling.
 constexpr int kTokPerCta = 8;
+constexpr int kGroups = 4;
 
-__device__ __forceinline__ float sum_partials(const float* p, int ksplit, size_t slice) {
-    float s = p[0];
-    int ks = 1;
-    for (; ks + 8 <= ksplit; ks += 8) {
+// sum of p[ks * slice] for ks = first, first + stride, ... < ksplit, in that order
+__device__ __forceinline__ float sum_partials(const float* p, int first, int stride, int ksplit, size_t slice) {
+    float s = 0.0f;
+    int ks = first;
+    for (; ks + 7 * stride < ksplit; ks += 8 * stride) {
         float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldg(p + (size_t)(ks + u) * slice);
+        for (int u = 0; u < 8; ++u) v[u] = __ldg(p + (size_t)(ks + u * stride) * slice);
 #pragma unroll
         for (int u = 0; u < 8; ++u) s += v[u];
     }
-    for (; ks < ksplit; ++ks) s += __ldg(p + (size_t)ks * slice);
+    for (; ks < ksplit; ks += stride) s += __ldg(p + (size_t)ks * slice);
     return s;
 }
 
 template <int EPL>  // logits per lane; expert e = i*32 + lane
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ partials, int ksplit,
+__global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ partials, int ksplit,
                                                    const float* __restrict__ bias, int T, int E, int k,
                                                    float* __restrict__ logits_out,
                                                    int32_t* __restrict__ topk_idx,
@@ -50,12 +54,28 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
     const size_t slice = (size_t)T * E;
     for (int t0 = blockIdx.x * tpc; t0 < T; t0 += gridDim.x * tpc) {
         const int nt = min(tpc, T - t0);
-        for (int q = threadIdx.x; q < nt * E; q += blockDim.x) {
-            const int tt = q / E, e = q - tt * E;
-            float s = sum_partials(partials + (size_t)(t0 + tt) * E + e, ksplit, slice);
-            if (bias) s += bias[e];
-            lg[tt][e] = s;
-            if (logits_out) logits_out[(size_t)(t0 + tt) * E + e] = s;
+        if (tpc == 1) {
+            // one token: group g of the CTA sums splits g, g + kGroups, ... into lg[g]
+            for (int q = threadIdx.x; q < kGroups * E; q += blockDim.x) {
+                const int g = q / E, e = q - g * E;
+                lg[g][e] = sum_partials(partials + (size_t)t0 * E + e, g, kGroups, ksplit, slice);
+            }
+            __syncthreads();
+            for (int e = threadIdx.x; e < E; e += blockDim.x) {
+                float s = lg[0][e];
+                for (int g = 1; g < kGroups && g < ksplit; ++g) s += lg[g][e];
+                if (bias) s += bias[e];
+                lg[0][e] = s;
+                if (logits_out) logits_out[(size_t)t0 * E + e] = s;
+            }
+        } else {
+            for (int q = threadIdx.x; q < nt * E; q += blockDim.x) {
+                const int tt = q / E, e = q - tt * E;
+                float s = sum_partials(partials + (size_t)(t0 + tt) * E + e, 0, 1, ksplit, slice);
+                if (bias) s += bias[e];
+                lg[tt][e] = s;
+                if (logits_out) logits_out[(size_t)(t0 + tt) * E + e] = s;
+            }
         }
         __syncthreads();
         if (warp < nt) {
@@ -156,8 +176,8 @@ template <int EPL>
 cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int T, int E, int k,
                        float* logits_out, int32_t* topk_idx, float* topk_w, int n_groups, int topk_groups,
                        cudaStream_t stream) {
-    const int threads = 256;
     const int tpc = T <= 4 * num_sms() ? 1 : kTokPerCta;
+    const int threads = tpc == 1 ? 1024 : 256;
     int blocks = (T + tpc - 1) / tpc;
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;

@@ -33,14 +33,19 @@ def _f32(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(DEV)
 
 
-def test_row_quantizer_is_bit_exact():
-    x = mi.normal_bf16((64, 7168), 1.0, 3, 40)
-    x[3] = 0
-    x[5, :] = mi.normal_bf16((7168,), 1e-3, 3, 41)
-    x[7, 11] = 1e4   # one outlier sets the scale
-    x[9] = mi.normal_bf16((7168,), 50.0, 3, 42)
-    codes = torch.empty((64, 7168), dtype=torch.uint8, device=DEV)
-    scale = torch.empty(64, dtype=torch.float32, device=DEV)
+@pytest.mark.parametrize("rows,cols", [(64, 7168), (300, 2048), (33, 4096), (5, 48), (7, 16384), (6, 16400)])
+def test_row_quantizer_is_bit_exact(rows, cols):
+    """Every row width the kernel distinguishes: one warp per row (2048, 48),
+    several warps per row through shared memory (4096, 7168, 16384), and rows
+    too wide for the registers of one CTA (16400)."""
+    x = mi.normal_bf16((rows, cols), 1.0, 3, 40)
+    x[min(3, rows - 1)] = 0
+    if rows > 5:
+        x[5, :] = mi.normal_bf16((cols,), 1e-3, 3, 41)
+        x[4, 11] = 1e4   # one outlier sets the scale
+        x[rows - 1] = mi.normal_bf16((cols,), 50.0, 3, 42)
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=DEV)
+    scale = torch.empty(rows, dtype=torch.float32, device=DEV)
     m.moe_quantize_rows_fp8(x.to(DEV), codes, scale)
     c_o, s_o = oracle.quantize_rows_e4m3(x)
     assert np.array_equal(scale.cpu().numpy(), s_o)
