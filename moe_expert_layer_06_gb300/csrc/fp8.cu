@@ -13,14 +13,43 @@
 namespace moe {
 namespace {
 
-// E4M3 codes of 8 bf16 values (one 16-byte vector) at scale s, packed into 8 bytes.
-__device__ __forceinline__ uint2 encode8(const uint4 q, float s) {
+// Row divisor: x / s correctly rounded (round to nearest even), as the
+// quantisation rule defines it.  For s >= 2^-96 the quotient comes from the
+// reciprocal r = RN(1/s) and one correction with the exact FMA residual:
+// q0 = RN(x r), e = x - q0 s (exact), q = RN(q0 + e r).  By Markstein's
+// theorem (a quotient within one ulp, corrected once with a reciprocal within
+// half an ulp, is the correctly rounded quotient, barring underflow and
+// overflow) this is RN(x / s); here |x| <= 448 s, so nothing overflows, and an
+// underflowing quotient is far below 2^-10, where every E4M3 code is a zero.
+// Smaller scales divide with __fdiv_rn.
+struct RowDiv {
+    float s, r;
+    bool fast;
+};
+
+__device__ __forceinline__ RowDiv row_div(float s) {
+    RowDiv d;
+    d.s = s;
+    d.r = __frcp_rn(s);
+    d.fast = s >= 0x1p-96f;
+    return d;
+}
+
+__device__ __forceinline__ float div_rn(const RowDiv& d, float x) {
+    if (!d.fast) return __fdiv_rn(x, d.s);
+    const float q0 = x * d.r;
+    const float e = fmaf(-q0, d.s, x);
+    return fmaf(e, d.r, q0);
+}
+
+// E4M3 codes of 8 bf16 values (one 16-byte vector) at a row's scale, packed into 8 bytes.
+__device__ __forceinline__ uint2 encode8(const uint4 q, const RowDiv& div) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     uint32_t packed[2] = {0, 0};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float lo = __fdiv_rn(__uint_as_float(w[i] << 16), s);
-        const float hi = __fdiv_rn(__uint_as_float(w[i] & 0xffff0000u), s);
+        const float lo = div_rn(div, __uint_as_float(w[i] << 16));
+        const float hi = div_rn(div, __uint_as_float(w[i] & 0xffff0000u));
         const uint32_t c0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
         const uint32_t c1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
         packed[i >> 1] |= (c0 | (c1 << 8)) << ((i & 1) * 16);
@@ -83,11 +112,12 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const uint
         const float s = row_scale(amax);
         if (live) {
             if (t == 0) scale[r] = s;
+            const RowDiv div = row_div(s);
             uint2* dst = codes + (size_t)r * vec_per_row;
 #pragma unroll
             for (int j = 0; j < kVpt; ++j) {
                 const int c = t + j * tpr;
-                if (c < vec_per_row) dst[c] = encode8(v[j], s);
+                if (c < vec_per_row) dst[c] = encode8(v[j], div);
             }
         }
     }
@@ -107,8 +137,9 @@ __global__ void __launch_bounds__(256) quantize_long_rows_kernel(const uint4* __
         for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
         const float s = row_scale(amax);
         if (lane == 0) scale[r] = s;
+        const RowDiv div = row_div(s);
         uint2* dst = codes + (size_t)r * vec_per_row;
-        for (int c = lane; c < vec_per_row; c += 32) dst[c] = encode8(__ldg(src + c), s);
+        for (int c = lane; c < vec_per_row; c += 32) dst[c] = encode8(__ldg(src + c), div);
     }
 }
 

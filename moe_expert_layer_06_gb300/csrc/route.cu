@@ -19,25 +19,25 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 // tpc (1..8) tokens per CTA, grid-stride: all threads sum the K-split partials
 // of the CTA's tokens (coalesced over experts, eight loads in flight) into
 // shared memory, then warp w runs the softmax and the k arg-max rounds of
-// token w.  Few tokens (decode) use one token per CTA of 1024 threads: each
-// logit's partials are summed by kGroups threads (group g takes splits g,
-// g + kGroups, ... in order) and the group sums added in group order, so the
-// result does not depend on scheduling.
+// token w.  Up to a few hundred tokens use one token per CTA; up to 64 tokens
+// (decode) the CTA has groups = 4 x 256 threads and each logit's partials are
+// summed by 4 threads (group g takes splits g, g + 4, ... in order) whose sums
+// are added in group order, so the result does not depend on scheduling.
 constexpr int kTokPerCta = 8;
-constexpr int kGroups = 4;
+constexpr int kMaxGroups = 4;
 
-// sum of p[ks * slice] for ks = first, first + stride, ... < ksplit, in that order
+// sum of p[ks * slice] for ks = first, first + stride, ... < ksplit, in that
+// order; eight loads in flight, the last block predicated
 __device__ __forceinline__ float sum_partials(const float* p, int first, int stride, int ksplit, size_t slice) {
     float s = 0.0f;
-    int ks = first;
-    for (; ks + 7 * stride < ksplit; ks += 8 * stride) {
+    for (int ks = first; ks < ksplit; ks += 8 * stride) {
         float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldg(p + (size_t)(ks + u * stride) * slice);
+        for (int u = 0; u < 8; ++u) v[u] = ks + u * stride < ksplit ? __ldg(p + (size_t)(ks + u * stride) * slice) : 0.0f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) s += v[u];
+        for (int u = 0; u < 8; ++u)
+            if (ks + u * stride < ksplit) s += v[u];
     }
-    for (; ks < ksplit; ks += stride) s += __ldg(p + (size_t)ks * slice);
     return s;
 }
 
@@ -46,8 +46,8 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ pa
                                                    const float* __restrict__ bias, int T, int E, int k,
                                                    float* __restrict__ logits_out,
                                                    int32_t* __restrict__ topk_idx,
-                                                   float* __restrict__ topk_w, int tpc, int n_groups,
-                                                   int topk_groups) {
+                                                   float* __restrict__ topk_w, int tpc, int groups,
+                                                   int n_groups, int topk_groups) {
     __shared__ float lg[kTokPerCta][EPL * 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -55,15 +55,15 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ pa
     for (int t0 = blockIdx.x * tpc; t0 < T; t0 += gridDim.x * tpc) {
         const int nt = min(tpc, T - t0);
         if (tpc == 1) {
-            // one token: group g of the CTA sums splits g, g + kGroups, ... into lg[g]
-            for (int q = threadIdx.x; q < kGroups * E; q += blockDim.x) {
+            // one token: group g of the CTA sums splits g, g + groups, ... into lg[g]
+            for (int q = threadIdx.x; q < groups * E; q += blockDim.x) {
                 const int g = q / E, e = q - g * E;
-                lg[g][e] = sum_partials(partials + (size_t)t0 * E + e, g, kGroups, ksplit, slice);
+                lg[g][e] = sum_partials(partials + (size_t)t0 * E + e, g, groups, ksplit, slice);
             }
             __syncthreads();
             for (int e = threadIdx.x; e < E; e += blockDim.x) {
                 float s = lg[0][e];
-                for (int g = 1; g < kGroups && g < ksplit; ++g) s += lg[g][e];
+                for (int g = 1; g < groups && g < ksplit; ++g) s += lg[g][e];
                 if (bias) s += bias[e];
                 lg[0][e] = s;
                 if (logits_out) logits_out[(size_t)t0 * E + e] = s;
@@ -177,13 +177,14 @@ cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int
                        float* logits_out, int32_t* topk_idx, float* topk_w, int n_groups, int topk_groups,
                        cudaStream_t stream) {
     const int tpc = T <= 4 * num_sms() ? 1 : kTokPerCta;
-    const int threads = tpc == 1 ? 1024 : 256;
+    const int groups = T <= 64 ? kMaxGroups : 1;
+    const int threads = 256 * groups;
     int blocks = (T + tpc - 1) / tpc;
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     topk_kernel<EPL><<<blocks, threads, 0, stream>>>(partials, ksplit, bias, T, E, k, logits_out, topk_idx,
-                                                     topk_w, tpc, n_groups, topk_groups);
+                                                     topk_w, tpc, groups, n_groups, topk_groups);
     return cudaGetLastError();
 }
 

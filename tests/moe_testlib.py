@@ -25,7 +25,19 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy()
 
 
-def assert_close(got, want, rel_frob=REL_FROB, elem_rms=ELEM_RMS, what=""):
+def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
+    """Half the bf16 spacing at |v| (8 significant bits): the rounding error a
+    bf16 output may carry on top of its arithmetic error."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 8).astype(np.int64))
+
+
+def assert_close(got, want, rel_frob=REL_FROB, elem_rms=ELEM_RMS, what="", bf16_out=True):
+    """Relative Frobenius error <= rel_frob and every |err| <= elem_rms * rms(want),
+    plus, for a bf16 output compared with the unrounded oracle, half the bf16
+    spacing at that element (a value between two bf16 numbers is at least
+    that far from both)."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
@@ -34,9 +46,14 @@ def assert_close(got, want, rel_frob=REL_FROB, elem_rms=ELEM_RMS, what=""):
     nw = np.linalg.norm(want)
     rel = np.linalg.norm(err) / nw if nw > 0 else np.linalg.norm(err)
     rms = np.sqrt(np.mean(want ** 2)) if want.size else 0.0
-    mx = np.abs(err).max() if err.size else 0.0
     assert rel <= rel_frob, f"{what}: relative Frobenius error {rel:.3e} > {rel_frob}"
-    assert mx <= elem_rms * rms + 1e-30, f"{what}: max |err| {mx:.3e} > {elem_rms}*rms ({rms:.3e})"
+    if err.size:
+        bound = elem_rms * rms + 1e-30 + (bf16_half_ulp(want) if bf16_out else 0.0)
+        worst = np.argmax(np.abs(err) - bound)
+        e_w, b_w = np.abs(err).ravel()[worst], np.broadcast_to(bound, err.shape).ravel()[worst]
+        assert e_w <= b_w, (f"{what}: |err| {e_w:.3e} > bound {b_w:.3e} ({elem_rms}*rms {elem_rms * rms:.3e}"
+                            f"{' + half bf16 ulp' if bf16_out else ''}) at value {want.ravel()[worst]:.4g}")
+    mx = np.abs(err).max() if err.size else 0.0
     return rel, mx / rms if rms else 0.0
 
 

@@ -52,6 +52,51 @@ def test_row_quantizer_is_bit_exact(rows, cols):
     assert np.array_equal(codes.cpu().numpy(), c_o)
 
 
+def _bf16_sweep_rows(n_rows=256, binades=20, seed=7):
+    """Rows holding every bf16 mantissa, both signs, in the `binades` binades at
+    and below the row maximum, zero-padded to a multiple of 16 columns.  Row
+    maxima: 448 * 2^k (power-of-two scales, so exact E4M3 ties occur), random
+    bf16 values, the extremes of the bf16 range, and scales on both sides of
+    2^-96."""
+    rng = np.random.default_rng(seed)
+    maxima = []
+    for r in range(n_rows):
+        if r % 2 == 0:
+            maxima.append(448.0 * 2.0 ** int(rng.integers(-120, 110)))
+        else:
+            maxima.append(float(torch.tensor(2.0 ** rng.uniform(-125, 126), dtype=torch.float32)
+                                .to(torch.bfloat16).float()))
+    maxima[:6] = [448.0 * 2.0 ** -96, 446.0 * 2.0 ** -96, 450.0 * 2.0 ** -96, 2.0 ** -130, 3.0e38, 448.0]
+    cols = ((2 * binades * 128 + 1 + 15) // 16) * 16
+    out = np.zeros((n_rows, cols), dtype=np.uint16)
+    for r, mx in enumerate(maxima):
+        mb = int(torch.tensor(mx, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).item()) & 0x7FFF
+        top = (mb >> 7) & 0xFF  # biased exponent of the maximum
+        vals = []
+        for eb in range(max(0, top - binades + 1), top + 1):
+            for mant in range(128):
+                b = (eb << 7) | mant
+                if b <= mb:
+                    vals += [b, b | 0x8000]
+        row = np.array(vals + [mb], dtype=np.uint16)
+        out[r, :len(row)] = row
+    return torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
+
+
+def test_row_quantizer_over_every_bf16_mantissa_is_bit_exact():
+    x = _bf16_sweep_rows()
+    rows, cols = x.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=DEV)
+    scale = torch.empty(rows, dtype=torch.float32, device=DEV)
+    m.moe_quantize_rows_fp8(x.to(DEV), codes, scale)
+    c_o, s_o = oracle.quantize_rows_e4m3(x)
+    assert np.array_equal(scale.cpu().numpy(), s_o)
+    got = codes.cpu().numpy()
+    assert np.array_equal(got, c_o), f"{int((got != c_o).sum())} codes differ"
+    # the sweep reaches exact ties: values halfway between two E4M3 codes at a power-of-two scale
+    assert any(float(s_) == 2.0 ** round(np.log2(float(s_))) for s_ in s_o)
+
+
 def _quantised_weights(w, rep=None):
     wg, wu, wd = mi.stacked_expert_weights(w, rep)
     sg, su, sd = mi.stacked_shared_weights(w)
@@ -119,7 +164,7 @@ def test_fp8_intermediate_and_down_stage(name, mode):
     y_o = np.stack([oracle.down_row_fp8(qh_o[r], sh_o[r], qd[s_], sd[s_]) for r, s_ in enumerate(slot_of_row)])
     assert_close(to_np(y), y_o, what=f"{name} FP8 down (routed)")
     ysh_o = np.stack([oracle.down_row_fp8(qhs_o[t], shs_o[t], q["qsd"], q["ssd"]) for t in range(T)])
-    assert_close(ysh.cpu().numpy().astype(np.float64), ysh_o, what=f"{name} FP8 down (shared)")
+    assert_close(ysh.cpu().numpy().astype(np.float64), ysh_o, what=f"{name} FP8 down (shared)", bf16_out=False)
 
 
 @pytest.mark.parametrize("name", ["tiny", "mid8", "rep8"])

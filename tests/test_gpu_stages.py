@@ -213,7 +213,7 @@ def test_expert_ffn_matches_oracle(name, mode):
     y_o = oracle.expert_ffn(w, T, offsets, xd, wg, wu, wd)
     assert_close(to_np(y_disp), y_o, what="y_disp")
     ysh_o = oracle.shared_rows(w, x, sg, su, sd)
-    assert_close(to_np(y_sh), ysh_o, what="y_shared")
+    assert_close(to_np(y_sh), ysh_o, what="y_shared", bf16_out=False)
 
 
 def test_gate_up_and_down_entry_points_compose_to_ffn():

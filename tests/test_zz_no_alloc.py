@@ -70,6 +70,6 @@ def test_noalloc_matches_workspace_entry_point_twice_in_a_row(name):
         m.moe_expert_ffn_noalloc(w, T, x, x_disp, offsets, wg, wu, wd, sg, su, sd, y, ys, m.MOE_FFN_AUTO)
         assert m.moe_check_status() == m.MOE_OK, m.last_error()
         assert_close(y.float().cpu().numpy(), y_ref.float().cpu().numpy(), what=f"{name} call {call} y_disp")
-        assert_close(ys.cpu().numpy(), ys_ref.cpu().numpy(), what=f"{name} call {call} y_shared")
+        assert_close(ys.cpu().numpy(), ys_ref.cpu().numpy(), what=f"{name} call {call} y_shared", bf16_out=False)
     del wg, wu, wd
     torch.cuda.empty_cache()
