@@ -225,10 +225,16 @@ MOE_API int moe_eplb_copy_replicas(const moe_shape_t* shape, const int32_t* host
  * that is 2*k*H*2 bytes per token (229,376 B at k=8, H=7168, section 2.3).
  * x [T,H] bf16; topk_idx [T,k]; replica_of [E] or NULL; outputs slot_of [T*k],
  * counts [S+1], block_counts [B] (or NULL), offsets [S+2], perm [T*k],
- * inv_perm [T*k] int32, x_disp [T*k,H] bf16. */
+ * inv_perm [T*k] int32, x_disp [T*k,H] bf16.  ws: device scratch of
+ * moe_dispatch_workspace_size(shape, T) bytes, 16-byte aligned (the size is 0,
+ * and ws may be NULL, below 4096 assignments; above, the index pass runs in
+ * chunks of 512 assignments with their histograms in ws), else
+ * MOE_ERR_WORKSPACE. */
+MOE_API size_t moe_dispatch_workspace_size(const moe_shape_t* shape, int T);
 MOE_API int moe_dispatch(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
                  const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
-                 int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* x_disp, void* stream);
+                 int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* x_disp, void* ws, size_t ws_bytes,
+                 void* stream);
 
 /* ---------------------------------------------------------------- step 3: expert FFN
  * Section 2.2 step 3 (each expert's FFN on its rows) with the SwiGLU form
@@ -296,7 +302,7 @@ MOE_API int moe_expert_ffn_noalloc(const moe_shape_t* shape, int T, const void* 
  * moe_quantize_rows_fp8: rows x cols bf16 -> codes [rows, cols] u8 and
  * scale [rows] fp32 (cols % 16 == 0).  Use it once on the expert gate and up
  * weights ([S*I, H] and [n_sh*I_sh, H]: one scale per output row).
- * moe_dispatch_fp8: moe_dispatch, except that each token is quantised once
+ * moe_dispatch_fp8: moe_dispatch (same workspace), except that each token is quantised once
  * (x8 [T,H] u8, x_scale [T]) and its dispatched copies carry its codes and
  * scale (x_disp8 [T*k,H] u8, x_disp_scale [T*k]): the dispatch buffer is
  * T*k*H bytes, half of the bf16 one (57,344 B per token at k=8, H=7168).
@@ -322,7 +328,8 @@ MOE_API int moe_quantize_rows_fp8(int rows, int cols, const void* x, uint8_t* co
 MOE_API int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
                              const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
                              int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint8_t* x8, float* x_scale,
-                             uint8_t* x_disp8, float* x_disp_scale, void* stream);
+                             uint8_t* x_disp8, float* x_disp_scale, void* ws, size_t ws_bytes,
+                             void* stream);
 MOE_API int moe_expert_gate_up_fp8(const moe_shape_t* shape, int T, const uint8_t* x8, const float* x_scale,
                                    const uint8_t* x_disp8, const float* x_disp_scale, const int32_t* offsets,
                                    const uint8_t* qg, const float* sg, const uint8_t* qu, const float* su,

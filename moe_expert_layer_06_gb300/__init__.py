@@ -38,7 +38,7 @@ EXPORTS = (
     "moe_workspace_size", "moe_forward", "moe_expert_ffn_noalloc", "moe_route_grouped",
     "moe_eplb_window_bytes", "moe_eplb_window_reset", "moe_eplb_window_push", "moe_eplb_stable_table",
     "moe_eplb_copy_replicas", "moe_quantize_rows_fp8", "moe_dispatch_fp8", "moe_expert_gate_up_fp8",
-    "moe_workspace_size_fp8", "moe_forward_fp8", "moe_expert_down_fp8",
+    "moe_workspace_size_fp8", "moe_forward_fp8", "moe_expert_down_fp8", "moe_dispatch_workspace_size",
 )
 
 # capacity of the fixed scratch of moe_expert_ffn_noalloc (include/moe.h)
@@ -83,7 +83,8 @@ _SIG = {
     "moe_eplb_stable_table": (_I, [_P, _P, _P, _P]),
     "moe_eplb_copy_replicas": (_I, [_P, _P, _P, _P, _P, _P, _P]),
     "moe_eplb_plan_replicas": (_I, [_P, _P, _I, _P]),
-    "moe_dispatch": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_dispatch_workspace_size": (_Z, [_P, _I]),
+    "moe_dispatch": (_I, [_P, _I] + [_P] * 10 + [_P, _Z, _P]),
     "moe_expert_gate_up": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_expert_down": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_ffn_workspace_size": (_Z, [_P, _I]),
@@ -91,7 +92,7 @@ _SIG = {
     "moe_expert_ffn_noalloc": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P]),
     "moe_combine": (_I, [_P, _I, _P, _P, _P, _P, _P, _P]),
     "moe_quantize_rows_fp8": (_I, [_I, _I, _P, _P, _P, _P]),
-    "moe_dispatch_fp8": (_I, [_P, _I] + [_P] * 13 + [_P]),
+    "moe_dispatch_fp8": (_I, [_P, _I] + [_P] * 13 + [_P, _Z, _P]),
     "moe_expert_gate_up_fp8": (_I, [_P, _I] + [_P] * 15 + [_I, _P]),
     "moe_workspace_size_fp8": (_Z, [_P, _I]),
     "moe_expert_down_fp8": (_I, [_P, _I] + [_P] * 11 + [_I, _P]),
@@ -242,11 +243,25 @@ def moe_eplb_copy_replicas(shape, old, new, w_gate, w_up, w_down, stream=None):
                                         _ptr(w_gate), _ptr(w_up), _ptr(w_down), _stream(stream)))
 
 
+def moe_dispatch_workspace_size(shape, T: int) -> int:
+    return lib().moe_dispatch_workspace_size(_shape(shape), T)
+
+
+def _dispatch_ws(shape, T, ws, like):
+    """The caller's dispatch workspace, or a fresh one on the device of `like`."""
+    if ws is not None:
+        return ws
+    n = moe_dispatch_workspace_size(shape, T)
+    return torch.empty(n, dtype=torch.uint8, device=like.device) if n else None
+
+
 def moe_dispatch(shape, T, x, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm,
-                 x_disp, stream=None):
+                 x_disp, ws=None, stream=None):
+    ws = _dispatch_ws(shape, T, ws, counts)
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(lib().moe_dispatch(_shape(shape), T, _ptr(x), _ptr(topk_idx), _ptr(replica_of), _ptr(slot_of),
                               _ptr(counts), _ptr(block_counts), _ptr(offsets), _ptr(perm), _ptr(inv_perm),
-                              _ptr(x_disp), _stream(stream)))
+                              _ptr(x_disp), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def moe_expert_gate_up(shape, T, x, x_disp, offsets, w_gate, w_up, ws_gate, ws_up, h_disp, h_shared,
@@ -310,10 +325,13 @@ def moe_quantize_rows_fp8(x, codes, scale, stream=None):
 
 
 def moe_dispatch_fp8(shape, T, x, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm,
-                     x8, x_scale, x_disp8, x_disp_scale, stream=None):
+                     x8, x_scale, x_disp8, x_disp_scale, ws=None, stream=None):
+    ws = _dispatch_ws(shape, T, ws, counts)
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(lib().moe_dispatch_fp8(_shape(shape), T, _ptr(x), _ptr(topk_idx), _ptr(replica_of), _ptr(slot_of),
                                   _ptr(counts), _ptr(block_counts), _ptr(offsets), _ptr(perm), _ptr(inv_perm),
-                                  _ptr(x8), _ptr(x_scale), _ptr(x_disp8), _ptr(x_disp_scale), _stream(stream)))
+                                  _ptr(x8), _ptr(x_scale), _ptr(x_disp8), _ptr(x_disp_scale), _ptr(ws), ws_bytes,
+                                  _stream(stream)))
 
 
 def moe_expert_gate_up_fp8(shape, T, x8, x_scale, x_disp8, x_disp_scale, offsets, qg, sg, qu, su, qsg, ssg, qsu,

@@ -15,6 +15,11 @@ namespace {
 
 constexpr int kIdxThreads = 1024;
 constexpr int kMaxSlots = 1024;
+// chunked index pass: from this many assignments, chunks of kIndexChunk
+// (more per chunk beyond kMaxIndexChunks chunks)
+constexpr int kChunkedIndexMin = 4096;
+constexpr int kIndexChunk = 512;
+constexpr int kMaxIndexChunks = 128;
 
 __device__ __forceinline__ int home_slot(int e, int E, int S, int n_blocks) {
     const int epb = E / n_blocks, spb = S / n_blocks;
@@ -41,28 +46,11 @@ __device__ __forceinline__ int slot_of_assignment(const DispatchArgs& a, int x, 
     return slot;
 }
 
-// One CTA: index work for all T*k assignments (a = t*k + j).  Warp w owns the
-// contiguous range [w*per, (w+1)*per) of assignments, so warp order is
-// assignment order.  Pass 1 counts per warp and slot; a scan over warps gives
-// each warp its first rank in every slot; pass 2 walks the range again in
-// order and hands out ranks (match_any groups equal slots within a step).
-__global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const DispatchArgs a) {
-    extern __shared__ int sm[];
-    const int NS = a.S + 1;    // slots + invalid bucket
-    int* cnt = sm;             // [NS]
-    int* base = cnt + NS;      // [NS + 1]
-    int* wc = base + NS + 1;   // [32][NS]: per-warp counts, then per-warp next rank
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = a.T * a.k;
-    const int per = (n + 31) / 32;
-    const int r0 = min(n, warp * per), r1 = min(n, r0 + per);
-    int* mine = wc + warp * NS;
-    const unsigned lt_mask = (1u << lane) - 1u;
-
-    for (int i = tid; i < 32 * NS; i += kIdxThreads) wc[i] = 0;
-    __syncthreads();
-
-    bool bad = false;
+// Pass 1 of a warp over its contiguous assignment range [r0, r1): slot of
+// each assignment (stored to slot_of when given) and this warp's count per
+// slot in mine[] (match_any groups equal slots within a step).
+__device__ __forceinline__ void warp_count_range(const DispatchArgs& a, int r0, int r1, int* mine, bool& bad) {
+    const int lane = threadIdx.x & 31;
     for (int x0 = r0; x0 < r1; x0 += 32) {
         const int x = x0 + lane;
         const bool valid = x < r1;
@@ -75,33 +63,45 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
         if (valid && (__ffs(peers) - 1) == lane) mine[slot] += __popc(peers);
         __syncwarp();
     }
-    if (bad) raise_status(a.st, kStatusInvalidExpert);
-    __syncthreads();
+}
 
-    // per slot: exclusive prefix over warps; totals are the counts
-    for (int s = tid; s < NS; s += kIdxThreads) {
-        int run = 0;
-        for (int w = 0; w < 32; ++w) {
-            const int c = wc[w * NS + s];
-            wc[w * NS + s] = run;
-            run += c;
+// Pass 2 over the same range in order: mine[slot] holds the next row of this
+// warp in each slot; rows are handed out in assignment order.
+__device__ __forceinline__ void warp_rank_range(const DispatchArgs& a, int r0, int r1, int* mine) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    bool unused = false;
+    for (int x0 = r0; x0 < r1; x0 += 32) {
+        const int x = x0 + lane;
+        const bool valid = x < r1;
+        const int slot = valid ? slot_of_assignment(a, x, unused) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, slot);
+        if (valid) {
+            const int row = mine[slot] + __popc(peers & lt_mask);
+            a.perm[row] = x;
+            a.inv_perm[x] = row;
         }
-        cnt[s] = run;
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) mine[slot] += __popc(peers);
+        __syncwarp();
     }
-    __syncthreads();
+}
 
-    for (int i = tid; i < NS; i += kIdxThreads) a.counts[i] = cnt[i];
+// From the per-slot totals cnt[NS]: counts, block loads and (when offsets is
+// given) the exclusive prefix base[0..NS] over slots and the invalid bucket,
+// written to offsets.  Called by every thread of the CTA.
+__device__ __forceinline__ void finish_counts(const DispatchArgs& a, const int* cnt, int* base, int NS) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < NS; i += blockDim.x) a.counts[i] = cnt[i];
     if (a.block_counts) {
         const int spb = a.S / a.n_blocks;
-        for (int b = tid; b < a.n_blocks; b += kIdxThreads) {
+        for (int b = tid; b < a.n_blocks; b += blockDim.x) {
             int sum = 0;
             for (int s = b * spb; s < (b + 1) * spb; ++s) sum += cnt[s];
             a.block_counts[b] = sum;
         }
     }
-    if (!a.offsets) return;  // histogram only
-
-    // exclusive prefix of counts over slots and the invalid bucket
+    if (!a.offsets) return;
     if (warp == 0) {
         const int ps = (NS + 31) / 32;
         const int s0 = min(NS, lane * ps), s1 = min(NS, s0 + ps);
@@ -121,23 +121,141 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
         if (lane == 31) base[NS] = incl;
     }
     __syncthreads();
-    for (int i = tid; i <= NS; i += kIdxThreads) a.offsets[i] = base[i];
+    for (int i = tid; i <= NS; i += blockDim.x) a.offsets[i] = base[i];
+}
 
-    bool bad2 = false;
-    for (int x0 = r0; x0 < r1; x0 += 32) {
-        const int x = x0 + lane;
-        const bool valid = x < r1;
-        const int slot = valid ? slot_of_assignment(a, x, bad2) : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, slot);
-        if (valid) {
-            const int row = base[slot] + mine[slot] + __popc(peers & lt_mask);
-            a.perm[row] = x;
-            a.inv_perm[x] = row;
+// One CTA: index work for all T*k assignments (a = t*k + j).  Warp w owns the
+// contiguous range [w*per, (w+1)*per) of assignments, so warp order is
+// assignment order.  Pass 1 counts per warp and slot; a scan over warps gives
+// each warp its first rank in every slot; pass 2 walks the range again in
+// order and hands out ranks.
+__global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const DispatchArgs a) {
+    extern __shared__ int sm[];
+    const int NS = a.S + 1;    // slots + invalid bucket
+    int* cnt = sm;             // [NS]
+    int* base = cnt + NS;      // [NS + 1]
+    int* wc = base + NS + 1;   // [32][NS]: per-warp counts, then per-warp next rank
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int n = a.T * a.k;
+    const int per = (n + 31) / 32;
+    const int r0 = min(n, warp * per), r1 = min(n, r0 + per);
+    int* mine = wc + warp * NS;
+
+    for (int i = tid; i < 32 * NS; i += kIdxThreads) wc[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    warp_count_range(a, r0, r1, mine, bad);
+    if (bad) raise_status(a.st, kStatusInvalidExpert);
+    __syncthreads();
+
+    // per slot: exclusive prefix over warps; totals are the counts
+    for (int s = tid; s < NS; s += kIdxThreads) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int c = wc[w * NS + s];
+            wc[w * NS + s] = run;
+            run += c;
         }
-        __syncwarp();
-        if (valid && (__ffs(peers) - 1) == lane) mine[slot] += __popc(peers);
-        __syncwarp();
+        cnt[s] = run;
     }
+    __syncthreads();
+    finish_counts(a, cnt, base, NS);
+    if (!a.offsets) return;  // histogram only
+    for (int s = tid; s < NS; s += kIdxThreads)
+        for (int w = 0; w < 32; ++w) wc[w * NS + s] += base[s];
+    __syncthreads();
+    warp_rank_range(a, r0, r1, mine);
+}
+
+// ---- many assignments: the same counting sort over chunks of kChunk
+// assignments, one CTA each, in three launches.  hist [chunks][NS] (the
+// caller's workspace) holds each chunk's count per slot, then the chunk's
+// first rank in each slot.
+constexpr int kChunkThreads = 256;
+constexpr int kChunkWarps = kChunkThreads / 32;
+
+__device__ __forceinline__ void chunk_range(int n, int chunk, int& lo, int& hi) {
+    lo = min(n, (int)blockIdx.x * chunk);
+    hi = min(n, lo + chunk);
+}
+
+// launch 1: per-chunk slot histograms (and slot_of)
+__global__ void __launch_bounds__(kChunkThreads) index_hist_kernel(const DispatchArgs a, int chunk,
+                                                                   int32_t* __restrict__ hist) {
+    extern __shared__ int sm[];
+    const int NS = a.S + 1;
+    int* cnt = sm;  // [NS]
+    for (int i = threadIdx.x; i < NS; i += kChunkThreads) cnt[i] = 0;
+    __syncthreads();
+    int lo, hi;
+    chunk_range(a.T * a.k, chunk, lo, hi);
+    bool bad = false;
+    for (int x = lo + (int)threadIdx.x; x < hi; x += kChunkThreads) {
+        const int slot = slot_of_assignment(a, x, bad);
+        if (a.slot_of) a.slot_of[x] = slot;
+        atomicAdd(&cnt[slot], 1);
+    }
+    if (bad) raise_status(a.st, kStatusInvalidExpert);
+    __syncthreads();
+    for (int i = threadIdx.x; i < NS; i += kChunkThreads) hist[(size_t)blockIdx.x * NS + i] = cnt[i];
+}
+
+// launch 2 (one CTA): per slot, exclusive prefix over chunks (in place) and the
+// totals; then counts, block loads and offsets
+__global__ void __launch_bounds__(kIdxThreads, 1) index_scan_kernel(const DispatchArgs a, int n_chunks,
+                                                                    int32_t* __restrict__ hist) {
+    extern __shared__ int sm[];
+    const int NS = a.S + 1;
+    int* cnt = sm;          // [NS]
+    int* base = cnt + NS;   // [NS + 1]
+    for (int s = threadIdx.x; s < NS; s += kIdxThreads) {
+        int run = 0;
+        for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = c0 + u < n_chunks ? hist[(size_t)(c0 + u) * NS + s] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (c0 + u < n_chunks) {
+                    hist[(size_t)(c0 + u) * NS + s] = run;
+                    run += v[u];
+                }
+            }
+        }
+        cnt[s] = run;
+    }
+    __syncthreads();
+    finish_counts(a, cnt, base, NS);
+}
+
+// launch 3: ranks within each chunk (per-warp ranges as in the one-CTA pass),
+// offset by the slot's offset and the chunk's first rank in the slot
+__global__ void __launch_bounds__(kChunkThreads) index_rank_kernel(const DispatchArgs a, int chunk,
+                                                                   const int32_t* __restrict__ hist) {
+    extern __shared__ int sm[];
+    const int NS = a.S + 1;
+    int* wc = sm;  // [kChunkWarps][NS]
+    const int tid = threadIdx.x, warp = tid >> 5;
+    int lo, hi;
+    chunk_range(a.T * a.k, chunk, lo, hi);
+    const int per = (hi - lo + kChunkWarps - 1) / kChunkWarps;
+    const int r0 = min(hi, lo + warp * per), r1 = min(hi, r0 + per);
+    int* mine = wc + warp * NS;
+    for (int i = tid; i < kChunkWarps * NS; i += kChunkThreads) wc[i] = 0;
+    __syncthreads();
+    bool unused = false;
+    warp_count_range(a, r0, r1, mine, unused);
+    __syncthreads();
+    for (int s = tid; s < NS; s += kChunkThreads) {
+        int run = a.offsets[s] + hist[(size_t)blockIdx.x * NS + s];
+        for (int w = 0; w < kChunkWarps; ++w) {
+            const int c = wc[w * NS + s];
+            wc[w * NS + s] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    warp_rank_range(a, r0, r1, mine);
 }
 
 // x_disp[row] = x[perm[row] / k] in 16-byte vectors.  A row is spread over
@@ -193,6 +311,42 @@ cudaError_t launch_index_pass(const DispatchArgs& a, cudaStream_t stream) {
         configured_device = dev;
     }
     index_pass_kernel<<<1, kIdxThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+int index_chunks(int n) {
+    if (n < kChunkedIndexMin) return 0;
+    int chunk = kIndexChunk;
+    if ((n + chunk - 1) / chunk > kMaxIndexChunks) chunk = (n + kMaxIndexChunks - 1) / kMaxIndexChunks;
+    return (n + chunk - 1) / chunk;
+}
+
+size_t index_workspace_bytes(int n, int n_slots) {
+    return (size_t)index_chunks(n) * (size_t)(n_slots + 1) * sizeof(int32_t);
+}
+
+cudaError_t launch_index_chunked(const DispatchArgs& a, int32_t* hist, cudaStream_t stream) {
+    const int n = a.T * a.k;
+    const int n_chunks = index_chunks(n);
+    const int chunk = (n + n_chunks - 1) / n_chunks;
+    const int NS = a.S + 1;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(index_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kChunkWarps * (kMaxSlots + 1) * sizeof(int)));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    index_hist_kernel<<<n_chunks, kChunkThreads, NS * sizeof(int), stream>>>(a, chunk, hist);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    index_scan_kernel<<<1, kIdxThreads, (2 * NS + 1) * sizeof(int), stream>>>(a, n_chunks, hist);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    index_rank_kernel<<<n_chunks, kChunkThreads, kChunkWarps * NS * sizeof(int), stream>>>(a, chunk, hist);
     return cudaGetLastError();
 }
 

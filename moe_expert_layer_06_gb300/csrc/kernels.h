@@ -105,6 +105,12 @@ struct DispatchArgs {
     DevStatus st;
 };
 cudaError_t launch_index_pass(const DispatchArgs& a, cudaStream_t stream);
+// The index pass in chunks (three launches) for large batches: index_chunks(n)
+// chunks (0: use launch_index_pass), with index_workspace_bytes(n, S) of
+// caller workspace for the per-chunk histograms.
+int index_chunks(int n);
+size_t index_workspace_bytes(int n, int n_slots);
+cudaError_t launch_index_chunked(const DispatchArgs& a, int32_t* hist, cudaStream_t stream);
 cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* perm, int n_rows, int k, int hidden,
                                 uint16_t* x_disp, cudaStream_t stream);
 int dispatch_max_slots();

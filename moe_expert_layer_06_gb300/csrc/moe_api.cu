@@ -266,9 +266,21 @@ static int route_impl(const moe_shape_t* s, int T, int n_groups, int topk_groups
 }
 
 // ------------------------------------------------------------------ dispatch
+static size_t dispatch_ws(const moe_shape_t* s, int T) {
+    return align256(index_workspace_bytes(T * s->top_k, s->n_slots));
+}
+
+// The index pass: one CTA, or in chunks for a large batch with a full
+// permutation (perm given), the per-chunk histograms in the workspace.
 static int index_impl(const moe_shape_t* s, int T, const int32_t* topk_idx, const int32_t* replica_of,
                       int32_t* slot_of, int32_t* counts, int32_t* block_counts, int32_t* offsets, int32_t* perm,
-                      int32_t* inv_perm, cudaStream_t stream) {
+                      int32_t* inv_perm, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const bool chunked = perm && index_chunks(T * s->top_k) > 0;
+    if (chunked) {
+        const size_t need = dispatch_ws(s, T);
+        if (!ws || ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "dispatch workspace %zu < %zu bytes", ws_bytes, need);
+        if (!aligned16(ws)) return fail(MOE_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+    }
     DevStatus st;
     int rc = device_status(&st);
     if (rc) return rc;
@@ -288,7 +300,10 @@ static int index_impl(const moe_shape_t* s, int T, const int32_t* topk_idx, cons
     d.perm = perm;
     d.inv_perm = inv_perm;
     d.st = st;
-    MOE_CUDA(launch_index_pass(d, stream), "index pass launch");
+    if (chunked)
+        MOE_CUDA(launch_index_chunked(d, static_cast<int32_t*>(ws), stream), "chunked index pass launch");
+    else
+        MOE_CUDA(launch_index_pass(d, stream), "index pass launch");
     return MOE_OK;
 }
 
@@ -530,7 +545,7 @@ static size_t ffn_ws(const moe_shape_t* s, int T) {
 
 // ------------------------------------------------------------------ forward workspace carving
 struct FwdLayout {
-    size_t route, idx, w, slot_of, perm, inv_perm, counts, blocks, offsets, x_disp, ffn, y_disp, y_sh, total;
+    size_t route, idx, w, slot_of, perm, inv_perm, counts, blocks, offsets, x_disp, ffn, y_disp, y_sh, dispatch, total;
 };
 
 static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
@@ -555,6 +570,7 @@ static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
     L.ffn = take(ffn_ws(s, T));
     L.y_disp = take(n * s->hidden * 2);
     L.y_sh = take((size_t)T * s->hidden * 4);
+    L.dispatch = take(dispatch_ws(s, T));
     L.total = off;
     return L;
 }
@@ -726,7 +742,7 @@ int moe_expert_histogram(const moe_shape_t* shape, int T, const int32_t* topk_id
     if (replica_of) NEED4(replica_of, "replica_of");
     if (block_counts) NEED4(block_counts, "block_counts");
     return index_impl(shape, T, topk_idx, replica_of, nullptr, counts, block_counts, nullptr, nullptr, nullptr,
-                      as_stream(stream));
+                      nullptr, 0, as_stream(stream));
 }
 
 double moe_eplb_imbalance(const int32_t* host_block_counts, int n_blocks) {
@@ -749,9 +765,14 @@ int moe_eplb_plan_replicas(const moe_shape_t* shape, const int32_t* host_expert_
     return plan_replicas_host(shape, host_expert_counts, n_rep, host_replica_of);
 }
 
+size_t moe_dispatch_workspace_size(const moe_shape_t* shape, int T) {
+    if (check_shape(shape, T)) return 0;
+    return dispatch_ws(shape, T);
+}
+
 int moe_dispatch(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx, const int32_t* replica_of,
                  int32_t* slot_of, int32_t* counts, int32_t* block_counts, int32_t* offsets, int32_t* perm,
-                 int32_t* inv_perm, void* x_disp, void* stream) {
+                 int32_t* inv_perm, void* x_disp, void* ws, size_t ws_bytes, void* stream) {
     int rc = check_shape(shape, T);
     if (rc) return rc;
     NEED4(counts, "counts");
@@ -770,8 +791,8 @@ int moe_dispatch(const moe_shape_t* shape, int T, const void* x, const int32_t* 
     NEED4(inv_perm, "inv_perm");
     NEED(x_disp, "x_disp");
     if (replica_of) NEED4(replica_of, "replica_of");
-    if ((rc = index_impl(shape, T, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm,
-                         as_stream(stream))))
+    if ((rc = index_impl(shape, T, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm, ws,
+                         ws_bytes, as_stream(stream))))
         return rc;
     MOE_CUDA(launch_scatter_rows(static_cast<const uint16_t*>(x), perm, T * shape->top_k, shape->top_k,
                                  shape->hidden, static_cast<uint16_t*>(x_disp), as_stream(stream)),
@@ -878,7 +899,7 @@ int moe_forward(const moe_shape_t* shape, int T, const void* x, const void* w_ro
                         stream)))
         return rc;
     if ((rc = moe_dispatch(shape, T, x, idx, replica_of, reinterpret_cast<int32_t*>(b + L.slot_of), counts, blocks,
-                           offsets, perm, inv, b + L.x_disp, stream)))
+                           offsets, perm, inv, b + L.x_disp, b + L.dispatch, dispatch_ws(shape, T), stream)))
         return rc;
     if ((rc = moe_expert_ffn(shape, T, x, b + L.x_disp, offsets, w_gate, w_up, w_down, ws_gate, ws_up, ws_down,
                              b + L.y_disp, y_sh, mode, b + L.ffn, ffn_ws(shape, T), stream)))
@@ -900,14 +921,14 @@ int moe_quantize_rows_fp8(int rows, int cols, const void* x, uint8_t* codes, flo
 int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
                      const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
                      int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint8_t* x8, float* x_scale,
-                     uint8_t* x_disp8, float* x_disp_scale, void* stream) {
+                     uint8_t* x_disp8, float* x_disp_scale, void* ws, size_t ws_bytes, void* stream) {
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (shape->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
     NEED4(counts, "counts");
     NEED4(offsets, "offsets");
     if (T == 0) return moe_dispatch(shape, 0, x, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm,
-                                    inv_perm, nullptr, stream);
+                                    inv_perm, nullptr, nullptr, 0, stream);
     NEED(x, "x");
     NEED4(topk_idx, "topk_idx");
     NEED4(slot_of, "slot_of");
@@ -919,7 +940,8 @@ int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32
     NEED4(x_disp_scale, "x_disp_scale");
     if (replica_of) NEED4(replica_of, "replica_of");
     cudaStream_t st = as_stream(stream);
-    if ((rc = index_impl(shape, T, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm, st)))
+    if ((rc = index_impl(shape, T, topk_idx, replica_of, slot_of, counts, block_counts, offsets, perm, inv_perm, ws,
+                         ws_bytes, st)))
         return rc;
     MOE_CUDA(launch_quantize_rows(static_cast<const uint16_t*>(x), T, shape->hidden, x8, x_scale, st),
              "quantize launch");
@@ -994,7 +1016,8 @@ int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* 
         return rc;
     if ((rc = moe_dispatch_fp8(shape, T, x, idx, replica_of, reinterpret_cast<int32_t*>(b + B.slot_of), counts,
                                blocks, offsets, perm, inv, b + L.x8, reinterpret_cast<float*>(b + L.x_scale),
-                               b + L.x_disp8, reinterpret_cast<float*>(b + L.x_disp_scale), stream)))
+                               b + L.x_disp8, reinterpret_cast<float*>(b + L.x_disp_scale), b + B.dispatch,
+                               dispatch_ws(shape, T), stream)))
         return rc;
     if ((rc = moe_expert_gate_up_fp8(shape, T, b + L.x8, reinterpret_cast<float*>(b + L.x_scale), b + L.x_disp8,
                                      reinterpret_cast<float*>(b + L.x_disp_scale), offsets, qg, sg, qu, su, qsg, ssg,

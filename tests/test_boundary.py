@@ -109,6 +109,19 @@ def test_pointer_and_workspace_validation_codes():
     assert L.moe_ffn_workspace_size(ctypes.byref(s), 32) == 32 * 8 * 2048 * 2 + 32 * 2 * 2048 * 2
     # combine: null output
     assert L.moe_combine(ctypes.byref(s), 4, b, b, b, None, None, None) == m.MOE_ERR_INVALID_ARG
+    # dispatch workspace: none below 4096 assignments, one histogram row of S+1 ints per 512-assignment chunk above
+    assert L.moe_dispatch_workspace_size(ctypes.byref(s), 511) == 0
+    assert L.moe_dispatch_workspace_size(ctypes.byref(s), 512) == ((8 * 257 * 4 + 255) // 256) * 256
+    assert L.moe_dispatch_workspace_size(ctypes.byref(s), 4096) == ((64 * 257 * 4 + 255) // 256) * 256
+    assert L.moe_dispatch_workspace_size(ctypes.byref(s), 65536) == ((128 * 257 * 4 + 255) // 256) * 256
+    need = L.moe_dispatch_workspace_size(ctypes.byref(s), 4096)
+    args = [ctypes.byref(s), 4096] + [b] * 10
+    assert L.moe_dispatch(*args, None, 0, None) == m.MOE_ERR_WORKSPACE
+    assert L.moe_dispatch(*args, b, need - 1, None) == m.MOE_ERR_WORKSPACE
+    assert L.moe_dispatch(*args, mis, need, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch_fp8(ctypes.byref(s), 4096, *([b] * 13), None, 0, None) == m.MOE_ERR_WORKSPACE
+    fw8 = L.moe_workspace_size_fp8(ctypes.byref(s), 4096)
+    assert fw8 >= L.moe_workspace_size(ctypes.byref(s), 4096) + 4096 * 8 * 7168
 
 
 def test_empty_batch_is_a_no_op():

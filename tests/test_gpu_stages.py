@@ -115,6 +115,12 @@ def _replica_plan(w):
 
 
 def _gpu_dispatch(w, x_dev, idx, replica_of):
+    r = _gpu_dispatch_raw(w, x_dev, idx, replica_of)
+    assert m.moe_check_status() == 0, m.last_error()
+    return r
+
+
+def _gpu_dispatch_raw(w, x_dev, idx, replica_of):
     T, k, S = w.tokens, w.top_k, w.n_slots
     n = T * k
     t32 = dict(dtype=torch.int32, device=DEV)
@@ -125,7 +131,6 @@ def _gpu_dispatch(w, x_dev, idx, replica_of):
     rep = torch.from_numpy(np.asarray(replica_of, np.int32)).to(DEV) if replica_of is not None else None
     m.moe_dispatch(w, T, x_dev, torch.from_numpy(np.ascontiguousarray(idx, np.int32)).to(DEV), rep,
                    r["slot_of"], r["counts"], r["blocks"], r["offsets"], r["perm"], r["inv"], r["x_disp"])
-    assert m.moe_check_status() == 0, m.last_error()
     return r
 
 
@@ -155,6 +160,46 @@ def test_dispatch_is_bit_exact(name):
         xs = x.view(torch.int16).numpy().view(np.uint16)
         rows = np.random.default_rng(0).choice(w.tokens * w.top_k, 2048, replace=False)
         assert np.array_equal(xg[rows], xs[perm[rows] // w.top_k])
+
+
+# the chunked index pass (4096 assignments and more): exactly at the threshold,
+# a ragged last chunk, and the 128-chunk cap (65600 assignments, 513 per chunk)
+# with replicas and out-of-range ids planted across chunk boundaries
+CHUNKED = {
+    "n4096": mi.WORKLOADS["tiny"].with_(name="n4096", tokens=512, hidden=16, n_experts=64, n_slots=64, top_k=8),
+    "n4104": mi.WORKLOADS["tiny"].with_(name="n4104", tokens=513, hidden=16, n_experts=64, n_slots=64, top_k=8),
+    "n65600": mi.WORKLOADS["tiny"].with_(name="n65600", tokens=8200, hidden=16, n_experts=256, n_slots=264,
+                                         n_blocks=8, top_k=8),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHUNKED))
+def test_chunked_index_pass_is_bit_exact(name):
+    w = CHUNKED[name]
+    T, k = w.tokens, w.top_k
+    rep = None
+    if w.n_slots > w.n_experts:
+        rep = oracle.plan_replicas(w, np.arange(w.n_experts)[::-1].copy(), w.n_slots - w.n_experts)
+    idx, _ = oracle.topk_softmax(mi.fp32_logits(w).double(), k)
+    idx = idx.copy()
+    bad = [(0, 0), (63, 7), (64, 0), (T // 2, 3), (T - 1, k - 1)]  # chunk edges at multiples of 512 / k tokens
+    for t, j in bad:
+        idx[t, j] = w.n_experts + t % 3 if t % 2 else -1 - t
+    x = mi.hidden_states(w)
+    assert m.moe_dispatch_workspace_size(w, T) > 0
+    g = _gpu_dispatch_raw(w, x.to(DEV), idx, rep)
+    assert m.moe_check_status() == m.MOE_ERR_DEVICE_STATUS  # the planted ids
+    so, n_bad = oracle.slot_map(w, idx, rep)
+    assert n_bad == len(bad)
+    counts, blocks = oracle.histogram(w, so)
+    offsets, perm, inv, xd = oracle.dispatch(w, T, so, counts, x)
+    assert np.array_equal(g["slot_of"].cpu().numpy(), so)
+    assert np.array_equal(g["counts"].cpu().numpy(), counts)
+    assert np.array_equal(g["blocks"].cpu().numpy(), blocks)
+    assert np.array_equal(g["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(g["perm"].cpu().numpy(), perm)
+    assert np.array_equal(g["inv"].cpu().numpy(), inv)
+    assert np.array_equal(g["x_disp"].cpu().view(torch.int16).numpy().view(np.uint16), xd)
 
 
 @pytest.mark.parametrize("name", ["tiny", "rep", "decode_t256_skew", "redundant_t1024"])
