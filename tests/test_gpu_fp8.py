@@ -167,9 +167,13 @@ def test_fp8_intermediate_and_down_stage(name, mode):
     assert_close(ysh.cpu().numpy().astype(np.float64), ysh_o, what=f"{name} FP8 down (shared)", bf16_out=False)
 
 
-@pytest.mark.parametrize("name", ["tiny", "mid8", "rep8"])
+# 4096 dispatched rows of 7168 bytes: the chunked index pass and the bulk-copy scatter
+BIG8 = mi.WORKLOADS["decode_t32"].with_(name="big8", tokens=512)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid8", "rep8", "big8"])
 def test_fp8_dispatch_is_bit_exact(name):
-    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "rep8": REP8}[name]
+    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "rep8": REP8, "big8": BIG8}[name]
     T, k, S, H = w.tokens, w.top_k, w.n_slots, w.hidden
     rep = None
     if w.n_slots > w.n_experts:
