@@ -35,24 +35,26 @@ __device__ __forceinline__ RowDiv row_div(float s) {
     return d;
 }
 
+template <bool FAST>
 __device__ __forceinline__ float div_rn(const RowDiv& d, float x) {
-    if (!d.fast) return __fdiv_rn(x, d.s);
+    if (!FAST) return __fdiv_rn(x, d.s);
     const float q0 = x * d.r;
     const float e = fmaf(-q0, d.s, x);
     return fmaf(e, d.r, q0);
 }
 
-// E4M3 codes of 8 bf16 values (one 16-byte vector) at a row's scale, packed into 8 bytes.
+// E4M3 codes of 8 bf16 values (one 16-byte vector) at a row's scale, packed
+// into 8 bytes in element order (two values per conversion).
+template <bool FAST>
 __device__ __forceinline__ uint2 encode8(const uint4 q, const RowDiv& div) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     uint32_t packed[2] = {0, 0};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float lo = div_rn(div, __uint_as_float(w[i] << 16));
-        const float hi = div_rn(div, __uint_as_float(w[i] & 0xffff0000u));
-        const uint32_t c0 = __nv_cvt_float_to_fp8(lo, __NV_SATFINITE, __NV_E4M3);
-        const uint32_t c1 = __nv_cvt_float_to_fp8(hi, __NV_SATFINITE, __NV_E4M3);
-        packed[i >> 1] |= (c0 | (c1 << 8)) << ((i & 1) * 16);
+        const float lo = div_rn<FAST>(div, __uint_as_float(w[i] << 16));
+        const float hi = div_rn<FAST>(div, __uint_as_float(w[i] & 0xffff0000u));
+        const uint32_t c = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+        packed[i >> 1] |= c << ((i & 1) * 16);
     }
     return make_uint2(packed[0], packed[1]);
 }
@@ -76,7 +78,7 @@ __device__ __forceinline__ float row_scale(float amax) { return amax > 0.0f ? __
 constexpr int kVpt = 8;
 constexpr int kQuantThreads = 256;
 
-__global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const uint4* __restrict__ x, int rows,
+__global__ void __launch_bounds__(kQuantThreads, 3) quantize_rows_kernel(const uint4* __restrict__ x, int rows,
                                                                       int vec_per_row, int tpr,
                                                                       uint2* __restrict__ codes,
                                                                       float* __restrict__ scale) {
@@ -114,10 +116,18 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const uint
             if (t == 0) scale[r] = s;
             const RowDiv div = row_div(s);
             uint2* dst = codes + (size_t)r * vec_per_row;
+            if (div.fast) {
 #pragma unroll
-            for (int j = 0; j < kVpt; ++j) {
-                const int c = t + j * tpr;
-                if (c < vec_per_row) dst[c] = encode8(v[j], div);
+                for (int j = 0; j < kVpt; ++j) {
+                    const int c = t + j * tpr;
+                    if (c < vec_per_row) dst[c] = encode8<true>(v[j], div);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVpt; ++j) {
+                    const int c = t + j * tpr;
+                    if (c < vec_per_row) dst[c] = encode8<false>(v[j], div);
+                }
             }
         }
     }
@@ -139,7 +149,10 @@ __global__ void __launch_bounds__(256) quantize_long_rows_kernel(const uint4* __
         if (lane == 0) scale[r] = s;
         const RowDiv div = row_div(s);
         uint2* dst = codes + (size_t)r * vec_per_row;
-        for (int c = lane; c < vec_per_row; c += 32) dst[c] = encode8(__ldg(src + c), div);
+        if (div.fast)
+            for (int c = lane; c < vec_per_row; c += 32) dst[c] = encode8<true>(__ldg(src + c), div);
+        else
+            for (int c = lane; c < vec_per_row; c += 32) dst[c] = encode8<false>(__ldg(src + c), div);
     }
 }
 
