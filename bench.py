@@ -246,7 +246,12 @@ def run_ours(args, rank, world, local_rank):
             m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh)
         m.moe_combine(w, T, y, inv, tw, ysh, out)
 
-    launches_per_step = (9 + (w.n_shared > 0)) if fp8 else 7
+    # router GEMM + top-k, index pass (three launches in chunks for large batches), scatter
+    # (E4M3: + token quantisation), gate/up, (E4M3: + intermediate quantisation), down, combine
+    index_launches = 3 if m.moe_dispatch_workspace_size(w, T) > 0 else 1
+    launches_per_step = 2 + index_launches + 1 + 1 + 1 + 1
+    if fp8:
+        launches_per_step += 1 + 1 + (w.n_shared > 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
