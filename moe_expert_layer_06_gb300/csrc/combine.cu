@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                                                       const float* __restrict__ topk_w,
                                                       const float4* __restrict__ y_shared, int T, int k,
                                                       int vec_per_row, uint4* __restrict__ out) {
+    pdl_begin();
     const size_t total = (size_t)T * vec_per_row;
     for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (size_t)gridDim.x * blockDim.x) {
@@ -91,10 +92,9 @@ cudaError_t launch_combine(const uint16_t* y_disp, const int32_t* inv_perm, cons
     size_t blocks = (total + 255) / 256;
     const size_t cap = (size_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    combine_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(y_disp), inv_perm, topk_w,
-                                                         reinterpret_cast<const float4*>(y_shared), T, k, vpr,
-                                                         reinterpret_cast<uint4*>(out));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                      reinterpret_cast<const uint4*>(y_disp), inv_perm, topk_w,
+                      reinterpret_cast<const float4*>(y_shared), T, k, vpr, reinterpret_cast<uint4*>(out));
 }
 
 }  // namespace moe

@@ -37,6 +37,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation (launch_pdl) and begins with pdl_begin():
+// its successor in the stream may launch once all of its CTAs have started,
+// and it waits for its predecessor to complete, memory included, before it
+// touches global memory.  Launch latency and CTA set-up overlap the
+// predecessor's tail; the order of every global access is that of a plain
+// stream.  The wait ends when the predecessor grid ends.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

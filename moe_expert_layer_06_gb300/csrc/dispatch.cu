@@ -130,6 +130,7 @@ __device__ __forceinline__ void finish_counts(const DispatchArgs& a, const int* 
 // each warp its first rank in every slot; pass 2 walks the range again in
 // order and hands out ranks.
 __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const DispatchArgs a) {
+    pdl_begin();
     extern __shared__ int sm[];
     const int NS = a.S + 1;    // slots + invalid bucket
     int* cnt = sm;             // [NS]
@@ -182,6 +183,7 @@ __device__ __forceinline__ void chunk_range(int n, int chunk, int& lo, int& hi) 
 // launch 1: per-chunk slot histograms (and slot_of)
 __global__ void __launch_bounds__(kChunkThreads) index_hist_kernel(const DispatchArgs a, int chunk,
                                                                    int32_t* __restrict__ hist) {
+    pdl_begin();
     extern __shared__ int sm[];
     const int NS = a.S + 1;
     int* cnt = sm;  // [NS]
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(kChunkThreads) index_hist_kernel(const Dispatc
 // totals; then counts, block loads and offsets
 __global__ void __launch_bounds__(kIdxThreads, 1) index_scan_kernel(const DispatchArgs a, int n_chunks,
                                                                     int32_t* __restrict__ hist) {
+    pdl_begin();
     extern __shared__ int sm[];
     const int NS = a.S + 1;
     int* cnt = sm;          // [NS]
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_scan_kernel(const Dispat
 // offset by the slot's offset and the chunk's first rank in the slot
 __global__ void __launch_bounds__(kChunkThreads) index_rank_kernel(const DispatchArgs a, int chunk,
                                                                    const int32_t* __restrict__ hist) {
+    pdl_begin();
     extern __shared__ int sm[];
     const int NS = a.S + 1;
     int* wc = sm;  // [kChunkWarps][NS]
@@ -268,6 +272,7 @@ __global__ void __launch_bounds__(kCopyThreads) scatter_rows_kernel(const uint4*
                                                                     const int32_t* __restrict__ perm, int n_rows,
                                                                     int k, int vec_per_row, int tpr,
                                                                     uint4* __restrict__ x_disp) {
+    pdl_begin();
     const int rows_per_cta = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int t0 = threadIdx.x - sub * tpr;
@@ -310,8 +315,7 @@ cudaError_t launch_index_pass(const DispatchArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    index_pass_kernel<<<1, kIdxThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(index_pass_kernel, dim3(1), dim3(kIdxThreads), smem, stream, a);
 }
 
 int index_chunks(int n) {
@@ -340,14 +344,12 @@ cudaError_t launch_index_chunked(const DispatchArgs& a, int32_t* hist, cudaStrea
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    index_hist_kernel<<<n_chunks, kChunkThreads, NS * sizeof(int), stream>>>(a, chunk, hist);
-    e = cudaGetLastError();
+    e = launch_pdl(index_hist_kernel, dim3(n_chunks), dim3(kChunkThreads), NS * sizeof(int), stream, a, chunk, hist);
     if (e != cudaSuccess) return e;
-    index_scan_kernel<<<1, kIdxThreads, (2 * NS + 1) * sizeof(int), stream>>>(a, n_chunks, hist);
-    e = cudaGetLastError();
+    e = launch_pdl(index_scan_kernel, dim3(1), dim3(kIdxThreads), (2 * NS + 1) * sizeof(int), stream, a, n_chunks, hist);
     if (e != cudaSuccess) return e;
-    index_rank_kernel<<<n_chunks, kChunkThreads, kChunkWarps * NS * sizeof(int), stream>>>(a, chunk, hist);
-    return cudaGetLastError();
+    return launch_pdl(index_rank_kernel, dim3(n_chunks), dim3(kChunkThreads), kChunkWarps * NS * sizeof(int), stream, a,
+                      chunk, static_cast<const int32_t*>(hist));
 }
 
 cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* perm, int n_rows, int k, int hidden,
@@ -360,9 +362,8 @@ cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* perm, int n_ro
     int blocks = (n_rows + rows_per_cta - 1) / rows_per_cta;
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    scatter_rows_kernel<<<blocks, kCopyThreads, 0, stream>>>(reinterpret_cast<const uint4*>(x), perm, n_rows, k,
-                                                            vec, tpr, reinterpret_cast<uint4*>(x_disp));
-    return cudaGetLastError();
+    return launch_pdl(scatter_rows_kernel, dim3(blocks), dim3(kCopyThreads), 0, stream,
+                      reinterpret_cast<const uint4*>(x), perm, n_rows, k, vec, tpr, reinterpret_cast<uint4*>(x_disp));
 }
 
 }  // namespace moe

@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(kThreads, 1) window_push_kernel(uint8_t* state
                                                                   double threshold, int64_t* block_load,
                                                                   int64_t* expert_load, double* ratio,
                                                                   int32_t* trigger) {
+    pdl_begin();
     __shared__ int64_t s_block[1024];
     WindowHeader* hdr = reinterpret_cast<WindowHeader*>(state);
     int32_t* ring = reinterpret_cast<int32_t*>(state + sizeof(WindowHeader));
@@ -127,11 +128,11 @@ int moe_eplb_window_push(const moe_shape_t* shape, int window, void* state, size
         return api_fail(MOE_ERR_WORKSPACE, "window state too small");
     if (!counts) return api_fail(MOE_ERR_INVALID_ARG, "counts is NULL");
     if (!(threshold > 0.0)) return api_fail(MOE_ERR_INVALID_ARG, "threshold must be > 0");
-    window_push_kernel<<<1, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint8_t*>(state), window, shape->n_slots, shape->n_experts, shape->n_blocks, counts, replica_of,
-        threshold, block_load, expert_load, ratio, trigger);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return api_fail(MOE_ERR_CUDA, "window push launch: %s", cudaGetErrorString(e));
+    const cudaError_t le = launch_pdl(window_push_kernel, dim3(1), dim3(kThreads), 0,
+                                      reinterpret_cast<cudaStream_t>(stream), static_cast<uint8_t*>(state), window,
+                                      shape->n_slots, shape->n_experts, shape->n_blocks, counts, replica_of, threshold,
+                                      block_load, expert_load, ratio, trigger);
+    if (le != cudaSuccess) return api_fail(MOE_ERR_CUDA, "window push launch: %s", cudaGetErrorString(le));
     return MOE_OK;
 }
 

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3) quantize_rows_kernel(const u
                                                                       int vec_per_row, int tpr,
                                                                       uint2* __restrict__ codes,
                                                                       float* __restrict__ scale) {
+    pdl_begin();
     __shared__ float part[kQuantThreads / 32];
     const int rows_per_cta = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;  // row slot of this thread in the CTA
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3) quantize_rows_kernel(const u
 __global__ void __launch_bounds__(256) quantize_long_rows_kernel(const uint4* __restrict__ x, int rows,
                                                                  int vec_per_row, uint2* __restrict__ codes,
                                                                  float* __restrict__ scale) {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < rows; r += gridDim.x * wpb) {
@@ -164,6 +166,7 @@ __global__ void __launch_bounds__(kQuantThreads) scatter_fp8_kernel(const uint4*
                                                                     int k, int vec_per_row, int tpr,
                                                                     uint4* __restrict__ out,
                                                                     float* __restrict__ out_scale) {
+    pdl_begin();
     const int rows_per_cta = blockDim.x / tpr;
     const int sub = threadIdx.x / tpr;
     const int t0 = threadIdx.x - sub * tpr;
@@ -200,9 +203,8 @@ cudaError_t launch_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t*
     if (vec > kVpt * kQuantThreads) {
         int blocks = (rows + 7) / 8;
         if (blocks > cap) blocks = cap;
-        quantize_long_rows_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), rows, vec,
-                                                              reinterpret_cast<uint2*>(codes), scale);
-        return cudaGetLastError();
+        return launch_pdl(quantize_long_rows_kernel, dim3(blocks), dim3(256), 0, stream,
+                          reinterpret_cast<const uint4*>(x), rows, vec, reinterpret_cast<uint2*>(codes), scale);
     }
     // threads per row: the fewest warps whose registers hold the row
     int tpr = 32;
@@ -210,9 +212,8 @@ cudaError_t launch_quantize_rows(const uint16_t* x, int rows, int cols, uint8_t*
     const int rows_per_cta = kQuantThreads / tpr;
     int blocks = (rows + rows_per_cta - 1) / rows_per_cta;
     if (blocks > cap) blocks = cap;
-    quantize_rows_kernel<<<blocks, kQuantThreads, 0, stream>>>(reinterpret_cast<const uint4*>(x), rows, vec, tpr,
-                                                               reinterpret_cast<uint2*>(codes), scale);
-    return cudaGetLastError();
+    return launch_pdl(quantize_rows_kernel, dim3(blocks), dim3(kQuantThreads), 0, stream,
+                      reinterpret_cast<const uint4*>(x), rows, vec, tpr, reinterpret_cast<uint2*>(codes), scale);
 }
 
 cudaError_t launch_scatter_fp8(const uint8_t* x8, const float* x_scale, const int32_t* perm, int n_rows, int k,
@@ -225,10 +226,9 @@ cudaError_t launch_scatter_fp8(const uint8_t* x8, const float* x_scale, const in
     int blocks = (n_rows + rows_per_cta - 1) / rows_per_cta;
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    scatter_fp8_kernel<<<blocks, kQuantThreads, 0, stream>>>(reinterpret_cast<const uint4*>(x8), x_scale, perm,
-                                                             n_rows, k, vec, tpr, reinterpret_cast<uint4*>(x_disp8),
-                                                             x_disp_scale);
-    return cudaGetLastError();
+    return launch_pdl(scatter_fp8_kernel, dim3(blocks), dim3(kQuantThreads), 0, stream,
+                      reinterpret_cast<const uint4*>(x8), x_scale, perm, n_rows, k, vec, tpr,
+                      reinterpret_cast<uint4*>(x_disp8), x_disp_scale);
 }
 
 }  // namespace moe

@@ -151,6 +151,7 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + _
 
 template <int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs a) {
+    pdl_begin();
     using C = Config<MODE, BN, STAGES>;
     constexpr int NA = C::NA;
     extern __shared__ uint8_t smem_raw[];
@@ -503,8 +504,7 @@ cudaError_t launch_one(const GemmArgs& args, int grid, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(args);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, args);
 }
 
 }  // namespace

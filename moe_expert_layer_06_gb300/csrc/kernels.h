@@ -7,10 +7,29 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 #include "common.cuh"
 
 namespace moe {
+
+// Launch `kern` with programmatic stream serialisation (see pdl_begin).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- grouped swap-AB GEMM (tcgen05)
 // kGateUpF8 / kDownF8: gate/up and down with E4M3 operands (128-element K

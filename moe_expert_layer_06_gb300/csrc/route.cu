@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ pa
                                                    int32_t* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w, int tpc, int groups,
                                                    int n_groups, int topk_groups) {
+    pdl_begin();
     __shared__ float lg[kTokPerCta][EPL * 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -183,9 +184,8 @@ cudaError_t launch_epl(const float* partials, int ksplit, const float* bias, int
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    topk_kernel<EPL><<<blocks, threads, 0, stream>>>(partials, ksplit, bias, T, E, k, logits_out, topk_idx,
-                                                     topk_w, tpc, groups, n_groups, topk_groups);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel<EPL>, dim3(blocks), dim3(threads), 0, stream, partials, ksplit, bias, T, E, k,
+                      logits_out, topk_idx, topk_w, tpc, groups, n_groups, topk_groups);
 }
 
 }  // namespace
