@@ -46,9 +46,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // predecessor's tail; the order of every global access is that of a plain
 // stream.  The wait ends when the predecessor grid ends.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void pdl_begin() {
+__device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_begin() {
+    pdl_launch_dependents();
+    pdl_wait();
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

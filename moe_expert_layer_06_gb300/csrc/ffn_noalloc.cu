@@ -60,6 +60,7 @@ extern "C" int moe_expert_ffn_noalloc(const moe_shape_t* shape, int T, const voi
                                       const void* w_down, const void* ws_gate, const void* ws_up,
                                       const void* ws_down, void* y_disp, float* y_shared, int mode,
                                       void* stream) {
+    moe::PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     using namespace moe;
     int rc = api_check_shape(shape, T);
     if (rc != MOE_OK) return rc;

@@ -151,7 +151,7 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + _
 
 template <int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs a) {
-    pdl_begin();
+    pdl_launch_dependents();
     using C = Config<MODE, BN, STAGES>;
     constexpr int NA = C::NA;
     extern __shared__ uint8_t smem_raw[];
@@ -170,6 +170,40 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const unsigned long long limit = a.st.limit_ns;
+
+    // ---- setup (reads nothing a predecessor writes): barriers, descriptors, TMEM
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int s = 0; s < C::kNumAcc; ++s) {
+            mbar_init(smem_u32(&tfull[s]), 1);
+            mbar_init(smem_u32(&tempty[s]), kEpiWarps);
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&a.a0);
+        tma_prefetch_desc(&a.b[0]);
+        if (NA == 2) tma_prefetch_desc(&a.a1);
+        if (MODE != kRouter && a.n_shared > 0) {
+            tma_prefetch_desc(&a.sa0);
+            tma_prefetch_desc(&a.sb[0]);
+            if (NA == 2) tma_prefetch_desc(&a.sa1);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    // ---- everything below reads the predecessor's results (offsets, activations)
+    pdl_wait();
 
     // ---- work list: shared items first, then routed items slot by slot
     int n_sh_items = 0;
@@ -205,38 +239,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncthreads();
         n_items = n_sh_items + tb.pre[a.n_slots];
     }
-    if ((int)blockIdx.x >= n_items) return;  // uniform across the CTA
-
-    // ---- setup: barriers, TMEM
-    if (warp == 0 && lane == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
-        }
-        for (int s = 0; s < C::kNumAcc; ++s) {
-            mbar_init(smem_u32(&tfull[s]), 1);
-            mbar_init(smem_u32(&tempty[s]), kEpiWarps);
-        }
-        mbar_init(smem_u32(mma_done), 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&a.a0);
-        tma_prefetch_desc(&a.b[0]);
-        if (NA == 2) tma_prefetch_desc(&a.a1);
-        if (MODE != kRouter && a.n_shared > 0) {
-            tma_prefetch_desc(&a.sa0);
-            tma_prefetch_desc(&a.sb[0]);
-            if (NA == 2) tma_prefetch_desc(&a.sa1);
-        }
+    if ((int)blockIdx.x >= n_items) {  // uniform across the CTA: nothing to do
+        if (warp == 1) tmem_dealloc(tbase, C::kTmemCols);
+        return;
     }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *tmem_slot;
 
     if (warp == 0) {
         // =========================== TMA producer ===========================

@@ -14,7 +14,24 @@
 
 namespace moe {
 
-// Launch `kern` with programmatic stream serialisation (see pdl_begin).
+// Programmatic dependent launch pays for small batches (launch gaps are a
+// visible part of a decode step) and costs a little for large ones (measured
+// on the same GPU: E4M3 decode T=32 0.9% faster, prefill T=4096 0.7% slower).
+// Each entry point of the C ABI turns it on for at most kPdlMaxAssignments
+// token-expert assignments (PdlScope); launch_pdl reads the calling thread's
+// setting.
+constexpr long kPdlMaxAssignments = 4096;
+bool pdl_enabled();
+
+struct PdlScope {
+    bool saved;
+    explicit PdlScope(long assignments);
+    ~PdlScope();
+};
+
+// Launch `kern`, with programmatic stream serialisation when enabled (the
+// kernels' pdl_begin is then their wait for the predecessor; otherwise it
+// returns at once).
 template <typename... Params, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                               Args&&... args) {
@@ -27,7 +44,7 @@ inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, si
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 

@@ -193,6 +193,13 @@ static int ffn_bn(int T, int mode) {
 
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+namespace {
+thread_local bool t_pdl = true;
+}
+bool pdl_enabled() { return t_pdl; }
+PdlScope::PdlScope(long assignments) : saved(t_pdl) { t_pdl = assignments <= kPdlMaxAssignments; }
+PdlScope::~PdlScope() { t_pdl = saved; }
+
 // ------------------------------------------------------------------ routing
 struct RoutePlan {
     int bn, ksplit, kc_split, tiles;
@@ -703,6 +710,7 @@ size_t moe_route_workspace_size(const moe_shape_t* shape, int T) {
 int moe_route(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
               const float* logits_in, float* logits_out, int32_t* topk_idx, float* topk_w, void* ws,
               size_t ws_bytes, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (T == 0) return MOE_OK;
@@ -713,6 +721,7 @@ int moe_route(const moe_shape_t* shape, int T, const void* x, const void* w_rout
 int moe_route_grouped(const moe_shape_t* shape, int T, int n_groups, int topk_groups, const void* x,
                       const void* w_router, const float* bias, const float* logits_in, float* logits_out,
                       int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (n_groups < 1 || n_groups > 32 || shape->n_experts % n_groups)
@@ -728,6 +737,7 @@ int moe_route_grouped(const moe_shape_t* shape, int T, int n_groups, int topk_gr
 
 int moe_expert_histogram(const moe_shape_t* shape, int T, const int32_t* topk_idx, const int32_t* replica_of,
                          int32_t* counts, int32_t* block_counts, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     NEED4(counts, "counts");
@@ -773,6 +783,7 @@ size_t moe_dispatch_workspace_size(const moe_shape_t* shape, int T) {
 int moe_dispatch(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx, const int32_t* replica_of,
                  int32_t* slot_of, int32_t* counts, int32_t* block_counts, int32_t* offsets, int32_t* perm,
                  int32_t* inv_perm, void* x_disp, void* ws, size_t ws_bytes, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     NEED4(counts, "counts");
@@ -803,6 +814,7 @@ int moe_dispatch(const moe_shape_t* shape, int T, const void* x, const int32_t* 
 int moe_expert_gate_up(const moe_shape_t* shape, int T, const void* x, const void* x_disp, const int32_t* offsets,
                        const void* w_gate, const void* w_up, const void* ws_gate, const void* ws_up, void* h_disp,
                        void* h_shared, int mode, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
@@ -814,6 +826,7 @@ int moe_expert_gate_up(const moe_shape_t* shape, int T, const void* x, const voi
 int moe_expert_down(const moe_shape_t* shape, int T, const void* h_disp, const void* h_shared,
                     const int32_t* offsets, const void* w_down, const void* ws_down, void* y_disp, float* y_shared,
                     int mode, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
@@ -831,6 +844,7 @@ int moe_expert_ffn(const moe_shape_t* shape, int T, const void* x, const void* x
                    const void* w_gate, const void* w_up, const void* w_down, const void* ws_gate, const void* ws_up,
                    const void* ws_down, void* y_disp, float* y_shared, int mode, void* ws, size_t ws_bytes,
                    void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
@@ -849,6 +863,7 @@ int moe_expert_ffn(const moe_shape_t* shape, int T, const void* x, const void* x
 
 int moe_combine(const moe_shape_t* shape, int T, const void* y_disp, const int32_t* inv_perm, const float* topk_w,
                 const float* y_shared, void* out, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (T == 0) return MOE_OK;
@@ -873,6 +888,7 @@ int moe_forward(const moe_shape_t* shape, int T, const void* x, const void* w_ro
                 const void* ws_gate, const void* ws_up, const void* ws_down, void* out, int32_t* topk_idx_out,
                 float* topk_w_out, int32_t* counts_out, int32_t* block_counts_out, int mode, void* ws,
                 size_t ws_bytes, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
@@ -908,6 +924,7 @@ int moe_forward(const moe_shape_t* shape, int T, const void* x, const void* w_ro
 }
 
 int moe_quantize_rows_fp8(int rows, int cols, const void* x, uint8_t* codes, float* scale, void* stream) {
+    PdlScope pdl((long)rows);
     if (rows < 0 || cols <= 0 || cols % 16) return fail(MOE_ERR_INVALID_ARG, "rows >= 0 and cols %% 16 == 0 required");
     if (rows == 0) return MOE_OK;
     NEED(x, "x");
@@ -922,6 +939,7 @@ int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32
                      const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
                      int32_t* offsets, int32_t* perm, int32_t* inv_perm, uint8_t* x8, float* x_scale,
                      uint8_t* x_disp8, float* x_disp_scale, void* ws, size_t ws_bytes, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (shape->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
@@ -956,6 +974,7 @@ int moe_expert_gate_up_fp8(const moe_shape_t* shape, int T, const uint8_t* x8, c
                            const uint8_t* qg, const float* sg, const uint8_t* qu, const float* su,
                            const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
                            void* h_disp, void* h_shared, int mode, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
@@ -968,6 +987,7 @@ int moe_expert_down_fp8(const moe_shape_t* shape, int T, const uint8_t* h8, cons
                         const float* hs_scale, const int32_t* offsets, const uint8_t* qd, const float* sd,
                         const uint8_t* qsd, const float* ssd, void* y_disp, float* y_shared, int mode,
                         void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
@@ -988,6 +1008,7 @@ int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* 
                     int32_t* topk_idx_out, float* topk_w_out,
                     int32_t* counts_out, int32_t* block_counts_out, int mode, void* ws, size_t ws_bytes,
                     void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
     int rc = check_shape(shape, T);
     if (rc) return rc;
     if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
