@@ -127,6 +127,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def routing_stats(w, counts_np, blocks_np, replica_of=None):
+    """Load statistics of one routed batch from the device histogram: rows per
+    slot, the share of assignments taken by the 30% most loaded experts, and
+    the EP-block imbalance max/mean with the replicas as placed and as if
+    every expert stayed in its home block."""
+    E, S, B = w.n_experts, w.n_slots, w.n_blocks
+    epb, spb = E // B, S // B
+    slot = counts_np[:S].astype(np.int64)
+    home = np.array([(e // epb) * spb + e % epb for e in range(E)])
+    expert = slot[home].copy()
+    if replica_of is not None:
+        for e, r in enumerate(replica_of):
+            if r >= 0:
+                expert[e] += slot[r]
+    total = max(1, int(expert.sum()))
+    top = np.sort(expert)[::-1][:max(1, (3 * E + 9) // 10)]
+    blocks = blocks_np.astype(np.int64)
+    home_blocks = expert.reshape(B, epb).sum(axis=1)
+    ratio = lambda b: float(b.max() * B / b.sum()) if b.sum() else 0.0
+    return {"max_rows_per_slot": int(slot.max()), "touched_experts": int((expert > 0).sum()),
+            "top30pct_expert_share": round(float(top.sum()) / total, 4),
+            "block_max_over_mean": round(ratio(blocks), 4),
+            "block_max_over_mean_without_replicas": round(ratio(home_blocks), 4)}
+
+
 def layer_bytes_flops(w, counts_np, fp8=False):
     """Algorithmic bytes and flops of one layer pass (touched expert weights read once).
 
@@ -387,6 +412,7 @@ def run_ours(args, rank, world, local_rank):
                    " (C ABI) with pinned host input/output copies in the timed region",
         },
         "gpu_launches": launches_per_step * args.steps,
+        "routing_stats": routing_stats(w, cnt, blocks.cpu().numpy(), rep),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
