@@ -31,6 +31,11 @@
  *     wait that expired) set a device status word instead of faulting;
  *     moe_check_status() synchronises the stream, reads and clears it.
  *   - T = 0 is valid and enqueues nothing.
+ *   - Calls of at most 4096 token-expert assignments (T*k) launch their
+ *     kernels with programmatic dependent launch: a kernel may be scheduled
+ *     while its predecessor in the stream finishes and waits for it before
+ *     touching memory, so results and memory order are those of plain stream
+ *     order (a caller's own kernel before it is waited for the same way).
  *
  * Notation: T tokens, H hidden, I routed intermediate, E routed experts,
  * k top-k, S slots (E, or E + redundant replicas), B blocks (EP ranks),
