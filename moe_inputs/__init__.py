@@ -197,6 +197,15 @@ WORKLOADS = {
                            description="prefill T=4096 (one 4k-token prompt), uniform routing"),
     "redundant_t1024": _dsv3("redundant_t1024", 1024, 1.5, n_slots=264,
                              description="T=1024 skewed routing, 256+8 slots, 8 hottest experts replicated"),
+    # more experts of the same shape (the group-limited routing row's 512/1024-expert scaling)
+    "decode_t32_e512": Workload(name="decode_t32_e512", tokens=32, hidden=7168, inter=2048, n_experts=512,
+                                top_k=8, n_shared=2, inter_shared=2048, n_slots=512, n_blocks=8,
+                                router_std=0.02, skew_alpha=0.0,
+                                description="decode T=32, DeepSeek-V3 expert shapes, 512 experts (8 blocks of 64)"),
+    "decode_t32_e1024": Workload(name="decode_t32_e1024", tokens=32, hidden=7168, inter=2048, n_experts=1024,
+                                 top_k=8, n_shared=2, inter_shared=2048, n_slots=1024, n_blocks=8,
+                                 router_std=0.02, skew_alpha=0.0,
+                                 description="decode T=32, DeepSeek-V3 expert shapes, 1024 experts (8 blocks of 128)"),
     # profiling cases: the same per-expert shapes and rows per expert with 32 experts
     # (2.8 GB of expert weights), small enough for multi-pass hardware-counter captures
     "decode_t32_e32": Workload(name="decode_t32_e32", tokens=32, hidden=7168, inter=2048, n_experts=32,

@@ -90,6 +90,24 @@ def check_topk(idx_gpu, idx_ref, logits_ref, k, gap=TOPK_GAP):
     return set_ok
 
 
+def grouped_sure(lo, k, G, Gk, gap=1e-4):
+    """Tokens whose group choice and expert choice (group-limited routing) are
+    both decided by more than gap, and the oracle's selection."""
+    T, E = lo.shape
+    gmax = -np.sort(-lo.reshape(T, G, E // G).max(axis=2), axis=1)
+    g_ok = (gmax[:, Gk - 1] - gmax[:, Gk]) > gap if Gk < G else np.ones(T, bool)
+    idx, _ = oracle.topk_grouped(lo, k, G, Gk)
+    masked = np.full_like(lo, -np.inf)
+    for t in range(T):
+        keep = sorted({int(e) // (E // G) for e in idx[t]} |
+                      set(np.argsort(-lo[t].reshape(G, E // G).max(axis=1), kind="stable")[:Gk].tolist()))
+        for g in keep:
+            masked[t, g * (E // G):(g + 1) * (E // G)] = lo[t, g * (E // G):(g + 1) * (E // G)]
+    s = -np.sort(-masked, axis=1)
+    e_ok = (s[:, k - 1] - s[:, k]) > gap if s.shape[1] > k else np.ones(T, bool)
+    return g_ok & e_ok, idx
+
+
 def parallel_router_logits(w, x_cpu, wr_cpu, bias):
     """Oracle logits for all rows, rows split across host threads (the C code is pure)."""
     T = x_cpu.shape[0]
@@ -135,16 +153,42 @@ class DeviceLayer:
         assert rc == 0, m.last_error()
         return dict(out=out, idx=idx, w=tw, counts=counts, blocks=blocks)
 
+    def forward_grouped(self, n_groups, topk_groups, mode=m.MOE_FFN_AUTO):
+        """The layer through the staged calls with group-limited routing."""
+        w, T, dev = self.w, self.w.tokens, self.dev
+        k, S, H, n = w.top_k, w.n_slots, w.hidden, w.tokens * w.top_k
+        i32 = dict(dtype=torch.int32, device=dev)
+        idx, tw = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
+        rws = torch.empty(max(16, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=dev)
+        m.moe_route_grouped(w, T, n_groups, topk_groups, self.x, self.wr, self.bias, None, None, idx, tw, rws)
+        so, counts, blocks = torch.empty(n, **i32), torch.empty(S + 1, **i32), torch.empty(w.n_blocks, **i32)
+        offsets, perm, inv = torch.empty(S + 2, **i32), torch.empty(n, **i32), torch.empty(n, **i32)
+        x_disp = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+        m.moe_dispatch(w, T, self.x, idx, self.replica_of, so, counts, blocks, offsets, perm, inv, x_disp)
+        y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
+        ysh = torch.empty((T, H), dtype=torch.float32, device=dev)
+        fws = torch.empty(max(16, m.moe_ffn_workspace_size(w, T)), dtype=torch.uint8, device=dev)
+        m.moe_expert_ffn(w, T, self.x, x_disp, offsets, self.wg, self.wu, self.wd, self.sg, self.su, self.sd, y,
+                         ysh if w.n_shared else None, mode, fws)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        m.moe_combine(w, T, y, inv, tw, ysh if w.n_shared else None, out)
+        assert m.moe_check_status() == 0, m.last_error()
+        return dict(out=out, idx=idx, w=tw, counts=counts, blocks=blocks)
 
-def oracle_token_rows(w, tokens, x_cpu, wr_cpu, bias, replica_of=None, expert_cache=None):
-    """Oracle routing and output for a sample of tokens of a full-size workload.
+
+def oracle_token_rows(w, tokens, x_cpu, wr_cpu, bias, replica_of=None, expert_cache=None, groups=None):
+    """Oracle routing and output for a sample of tokens of a full-size workload
+    (groups = (n_groups, topk_groups) for group-limited routing).
 
     Only the experts those tokens select are generated (on the CPU).
     """
     expert_cache = {} if expert_cache is None else expert_cache
     xs = x_cpu[tokens]
     logits = oracle.router_logits(w, xs, wr_cpu, bias)
-    idx, wt = oracle.topk_softmax(logits, w.top_k)
+    if groups is None:
+        idx, wt = oracle.topk_softmax(logits, w.top_k)
+    else:
+        idx, wt = oracle.topk_grouped(logits, w.top_k, *groups)
     need = sorted(set(int(e) for e in idx.ravel()) - set(expert_cache))
     for e in need:
         expert_cache[e] = mi.expert_weights(w, e)

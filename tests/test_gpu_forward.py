@@ -13,7 +13,7 @@ import torch
 import moe_expert_layer_06_gb300 as m
 import moe_inputs as mi
 import oracle
-from moe_testlib import (DeviceLayer, assert_close, check_topk, oracle_token_rows, parallel_router_logits,
+from moe_testlib import (grouped_sure, DeviceLayer, assert_close, check_topk, oracle_token_rows, parallel_router_logits,
                          to_np)
 from test_gpu_stages import DEEP, MID, REP
 
@@ -129,4 +129,27 @@ def test_redundant_experts_full_size(dsv3_weights):
     diff = (r["out"].float() - r0["out"].float()).abs().max().item()
     assert diff == 0.0, f"replicated vs plain layer differ by {diff}"
     del weights
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("groups", [None, (8, 4)])
+def test_forward_full_size_1024_experts(groups):
+    """1024 experts of the DeepSeek-V3 shape (90 GB of bf16 weights), plain and
+    group-limited routing (8 groups, 4 kept): sampled tokens against the oracle."""
+    w = mi.WORKLOADS["decode_t32_e1024"]
+    weights = mi.stacked_expert_weights(w, device=DEV)
+    layer = DeviceLayer(w, DEV, weights=weights)
+    if groups is None:
+        _check_full(w, layer, n_sample=2)
+    else:
+        T, k = w.tokens, w.top_k
+        r = layer.forward_grouped(*groups)
+        x, wr = mi.hidden_states(w), mi.router_weight(w)
+        lo = parallel_router_logits(w, x, wr, None)
+        sure, idx_o = grouped_sure(lo, k, *groups)
+        assert np.array_equal(r["idx"].cpu().numpy()[sure], idx_o[sure])
+        toks = _sample_tokens(T, sure, 2)
+        ref = oracle_token_rows(w, toks, x, wr, None, None, _EXPERTS_CPU, groups=groups)
+        assert_close(to_np(r["out"])[toks], ref["out"], what="1024 experts, group-limited, sampled out")
+    del weights, layer
     torch.cuda.empty_cache()

@@ -11,7 +11,7 @@ import torch
 import moe_expert_layer_06_gb300 as m
 import moe_inputs as mi
 import oracle
-from moe_testlib import assert_close, to_np
+from moe_testlib import grouped_sure as _grouped_sure, assert_close, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -322,23 +322,6 @@ def test_grouped_topk_from_fp32_logits_is_bit_exact(name, G, Gk):
     np.testing.assert_allclose(tw.cpu().numpy(), wt_o, rtol=2e-6, atol=1e-9)
     gs = w.n_experts // G
     assert all(len({int(e) // gs for e in row}) <= Gk for row in idx_o)
-
-
-def _grouped_sure(lo, k, G, Gk, gap=1e-4):
-    """Tokens whose group choice and expert choice are both decided by more than gap."""
-    T, E = lo.shape
-    gmax = -np.sort(-lo.reshape(T, G, E // G).max(axis=2), axis=1)
-    g_ok = (gmax[:, Gk - 1] - gmax[:, Gk]) > gap if Gk < G else np.ones(T, bool)
-    idx, _ = oracle.topk_grouped(lo, k, G, Gk)
-    masked = np.full_like(lo, -np.inf)
-    for t in range(T):
-        keep = sorted({int(e) // (E // G) for e in idx[t]} |
-                      set(np.argsort(-lo[t].reshape(G, E // G).max(axis=1), kind="stable")[:Gk].tolist()))
-        for g in keep:
-            masked[t, g * (E // G):(g + 1) * (E // G)] = lo[t, g * (E // G):(g + 1) * (E // G)]
-    s = -np.sort(-masked, axis=1)
-    e_ok = (s[:, k - 1] - s[:, k]) > gap if s.shape[1] > k else np.ones(T, bool)
-    return g_ok & e_ok, idx
 
 
 @pytest.mark.parametrize("name,G,Gk", [("mid", 4, 2), ("decode_t32", 8, 4), ("prefill_t4096", 8, 3)])
