@@ -9,10 +9,15 @@
 // expert).  So the weight matrix is the UMMA "A" operand (M = 128 output
 // rows per tile) and the expert's token rows the "B" operand (N = up to BN
 // rows, rounded up to 16): each weight tile streams from HBM once per token
-// chunk, and with BN = 256 each expert's weights are read exactly once up to
-// 256 rows per expert.
+// chunk.  BN is 32 at decode (five 36 KB pipeline stages) and 160 above 32
+// tokens (four 52 KB stages), which covers every expert of a 4096-token
+// batch with uniform routing in one chunk; the chunks of one expert that
+// needs more run at the same time on different SMs and share its weights
+// through L2.
 //
-// Work item = (matrix, 128-row block of outputs, token chunk[, K split]).
+// Work item = (matrix, 128-row block of outputs, token chunk[, K split]);
+// a gate/up item carries the gate and the up tile of the same rows, a down
+// item two consecutive 128-row tiles.  E4M3 modes use 128-element K chunks.
 // The item list is derived on the device from the dispatch offsets, so no
 // host synchronisation is needed.  A persistent CTA per SM takes items
 // round-robin; warp roles:

@@ -582,7 +582,8 @@ static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
     return L;
 }
 
-// FP8 forward: the bf16 layout plus the quantised tokens and their dispatched copies
+// FP8 forward: the bf16 layout plus the quantised tokens, their dispatched copies and the
+// quantised intermediates (routed rows, shared rows)
 struct FwdLayoutF8 {
     FwdLayout base;
     size_t x8, x_scale, x_disp8, x_disp_scale, h8, h_scale, hs8, hs_scale, total;
