@@ -5,7 +5,8 @@
 // router logits; step 5 weights each selected expert's output by
 // softmax(logits)[i].  The softmax runs over all E logits and the selected
 // probabilities are not renormalised.  Selection is by value, ties broken by
-// the lower expert index, using warp-shuffle arg-max rounds.
+// the lower expert index: by warp-shuffle arg-max rounds, or, for a decode
+// batch of at most 256 experts, by each thread ranking its expert against all.
 #include "kernels.h"
 
 namespace moe {
@@ -24,6 +25,11 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
 // summed by 4 threads (group g takes splits g, g + 4, ... in order) whose sums
 // are added in group order, so the result does not depend on scheduling.
 constexpr int kTokPerCta = 8;
+// up to 64 tokens (one token per 1024-thread CTA) and at most this many
+// experts: selection by ranks (measured ~1 us faster than the warp's k
+// arg-max rounds there; slower at 256 tokens, where 256-thread CTAs keep the
+// warp rounds)
+constexpr int kRankMaxExperts = 256;
 constexpr int kMaxGroups = 4;
 
 // sum of p[ks * slice] for ks = first, first + stride, ... < ksplit, in that
@@ -49,7 +55,8 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ pa
                                                    float* __restrict__ topk_w, int tpc, int groups,
                                                    int n_groups, int topk_groups) {
     pdl_begin();
-    __shared__ float lg[kTokPerCta][EPL * 32];
+    __shared__ __align__(16) float lg[kTokPerCta][EPL * 32];
+    __shared__ float red[32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const size_t slice = (size_t)T * E;
@@ -79,6 +86,54 @@ __global__ void __launch_bounds__(1024) topk_kernel(const float* __restrict__ pa
             }
         }
         __syncthreads();
+        if (groups > 1 && topk_groups >= n_groups && E <= kRankMaxExperts && E <= (int)blockDim.x) {
+            // one token, plain top-k: thread e ranks expert e against all E
+            // (larger logit first, equal logits by lower index); ranks below
+            // k are the selection in order.  Softmax statistics by block
+            // reductions in a fixed order.
+            const int e = threadIdx.x;
+            const int nw = (E + 31) / 32;  // warps that hold experts
+            const float v = e < E ? lg[0][e] : -INFINITY;
+            float m_ = v;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) m_ = fmaxf(m_, __shfl_xor_sync(0xffffffffu, m_, d));
+            if (lane == 0 && warp < nw) red[warp] = m_;
+            __syncthreads();
+            float mx = red[0];
+            for (int w = 1; w < nw; ++w) mx = fmaxf(mx, red[w]);
+            const float ex = e < E ? expf(v - mx) : 0.0f;
+            float sum = ex;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, d);
+            __syncthreads();  // every thread has read the maxima
+            if (lane == 0 && warp < nw) red[warp] = sum;
+            __syncthreads();
+            float den = 0.0f;
+            for (int w = 0; w < nw; ++w) den += red[w];
+            if (e < E) {
+                // four logits per (broadcast) shared-memory read, several reads in flight
+                const float4* row4 = reinterpret_cast<const float4*>(lg[0]);
+                int rank = 0, j = 0;
+#pragma unroll 4
+                for (; j + 4 <= E; j += 4) {
+                    const float4 u = row4[j >> 2];
+                    rank += (u.x > v || (u.x == v && j < e)) ? 1 : 0;
+                    rank += (u.y > v || (u.y == v && j + 1 < e)) ? 1 : 0;
+                    rank += (u.z > v || (u.z == v && j + 2 < e)) ? 1 : 0;
+                    rank += (u.w > v || (u.w == v && j + 3 < e)) ? 1 : 0;
+                }
+                for (; j < E; ++j) {
+                    const float u = lg[0][j];
+                    rank += (u > v || (u == v && j < e)) ? 1 : 0;
+                }
+                if (rank < k) {
+                    topk_idx[(size_t)t0 * k + rank] = e;
+                    topk_w[(size_t)t0 * k + rank] = ex * (1.0f / den);
+                }
+            }
+            __syncthreads();  // lg and red are rewritten for the next token
+            continue;
+        }
         if (warp < nt) {
             const int t = t0 + warp;
             float v[EPL];
