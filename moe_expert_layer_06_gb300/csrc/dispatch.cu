@@ -138,11 +138,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
     int* wc = base + NS + 1;   // [32][NS]: per-warp counts, then per-warp next rank
     const int tid = threadIdx.x, warp = tid >> 5;
     const int n = a.T * a.k;
-    const int per = (n + 31) / 32;
-    const int r0 = min(n, warp * per), r1 = min(n, r0 + per);
-    int* mine = wc + warp * NS;
+    // warps that own assignments: one 32-wide step each while there are few
+    const int nw = min(32, max(1, (n + 31) / 32));
+    const int per = (n + nw - 1) / nw;
+    const int r0 = warp < nw ? min(n, warp * per) : n, r1 = warp < nw ? min(n, r0 + per) : n;
+    int* mine = wc + min(warp, nw - 1) * NS;  // warps >= nw have empty ranges
 
-    for (int i = tid; i < 32 * NS; i += kIdxThreads) wc[i] = 0;
+    for (int i = tid; i < nw * NS; i += kIdxThreads) wc[i] = 0;
     __syncthreads();
     bool bad = false;
     warp_count_range(a, r0, r1, mine, bad);
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
     // per slot: exclusive prefix over warps; totals are the counts
     for (int s = tid; s < NS; s += kIdxThreads) {
         int run = 0;
-        for (int w = 0; w < 32; ++w) {
+        for (int w = 0; w < nw; ++w) {
             const int c = wc[w * NS + s];
             wc[w * NS + s] = run;
             run += c;
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) index_pass_kernel(const Dispat
     finish_counts(a, cnt, base, NS);
     if (!a.offsets) return;  // histogram only
     for (int s = tid; s < NS; s += kIdxThreads)
-        for (int w = 0; w < 32; ++w) wc[w * NS + s] += base[s];
+        for (int w = 0; w < nw; ++w) wc[w * NS + s] += base[s];
     __syncthreads();
     warp_rank_range(a, r0, r1, mine);
 }
