@@ -391,20 +391,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const bool row_ok = mrow < mlim;
             (void)row_ok;
             const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + acc * C::kAccCols;
-            for (int g = part; g < nb; g += kEpiWarps / 4) {
-                float v0[16], v1[16];
-                tmem_ld16(tl + g * 16, v0);
-                if (NA == 2) tmem_ld16(tl + BN + g * 16, v1);
-                tmem_ld_wait();
-                if (Traits<MODE>::kGateUpLike) {
-                    if (row_ok) {
-                        if (MODE == kGateUpF8) {
+            if (Traits<MODE>::kGateUpLike) {
+                // SwiGLU per column group into packed bf16 registers, then free the
+                // accumulator (the next item's MMAs may start) and store
+                constexpr int kMaxG = (BN / 16 + kEpiWarps / 4 - 1) / (kEpiWarps / 4);
+                uint32_t hp[kMaxG][8];
+                const float* sa0 = nullptr;
+                const float* sa1 = nullptr;
+                const float* sbp = nullptr;
+                if (MODE == kGateUpF8) {
+                    sa0 = it.shared ? a.sa0_scale + (size_t)it.z * a.m_shared : a.a0_scale + (size_t)it.z * a.m_routed;
+                    sa1 = it.shared ? a.sa1_scale + (size_t)it.z * a.m_shared : a.a1_scale + (size_t)it.z * a.m_routed;
+                    sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
+                }
+#pragma unroll
+                for (int gi = 0; gi < kMaxG; ++gi) {
+                    const int g = part + gi * (kEpiWarps / 4);
+                    if (g < nb) {
+                        float v0[16], v1[16];
+                        tmem_ld16(tl + g * 16, v0);
+                        tmem_ld16(tl + BN + g * 16, v1);
+                        tmem_ld_wait();
+                        if (MODE == kGateUpF8 && row_ok) {
                             // dequantise: weight-row scale x token scale (both factor out of the K sum)
-                            const float* sa0 = it.shared ? a.sa0_scale + (size_t)it.z * a.m_shared
-                                                         : a.a0_scale + (size_t)it.z * a.m_routed;
-                            const float* sa1 = it.shared ? a.sa1_scale + (size_t)it.z * a.m_shared
-                                                         : a.a1_scale + (size_t)it.z * a.m_routed;
-                            const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
                             const float wg = __ldg(sa0 + mrow), wu = __ldg(sa1 + mrow);
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
@@ -414,70 +423,97 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                                 v1[j] *= wu * sx;
                             }
                         }
-                        __nv_bfloat16* dst;
-                        int ld;
-                        if (it.shared) {
-                            dst = reinterpret_cast<__nv_bfloat16*>(a.out_sh) + (size_t)it.z * a.sh_col_stride + mrow;
-                            ld = a.out_sh_ld;
-                        } else {
-                            dst = reinterpret_cast<__nv_bfloat16*>(a.out) + mrow;
-                            ld = a.out_ld;
-                        }
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int col = g * 16 + j;
-                            if (col < it.nrows)
-                                dst[(size_t)(it.row0 + col) * ld] = __float2bfloat16_rn(silu_f(v0[j]) * v1[j]);
+                        for (int j = 0; j < 8; ++j) {
+                            const __nv_bfloat162 p2 = __floats2bfloat162_rn(silu_f(v0[2 * j]) * v1[2 * j],
+                                                                            silu_f(v0[2 * j + 1]) * v1[2 * j + 1]);
+                            hp[gi][j] = *reinterpret_cast<const uint32_t*>(&p2);
                         }
                     }
-                } else {
-                    // FP8 down: the token-row scales of this column group
-                    float sxv[16];
-                    if (MODE == kDownF8) {
-                        const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int col = g * 16 + j;
-                            sxv[j] = col < it.nrows ? __ldg(sbp + col) : 0.0f;
-                        }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+                if (row_ok) {
+                    uint16_t* dst;
+                    int ld;
+                    if (it.shared) {
+                        dst = reinterpret_cast<uint16_t*>(a.out_sh) + (size_t)it.z * a.sh_col_stride + mrow;
+                        ld = a.out_sh_ld;
+                    } else {
+                        dst = reinterpret_cast<uint16_t*>(a.out) + mrow;
+                        ld = a.out_ld;
                     }
-                    // NA consecutive 128-row output blocks (down: rows m0.. and m0+128..)
 #pragma unroll
-                    for (int hh = 0; hh < NA; ++hh) {
-                        const int row = mrow + hh * 128;
-                        if (row >= mlim) continue;
-                        if (MODE == kDownF8) {
-                            // dequantise: weight-row scale x intermediate-row scale
-                            const float sw = it.shared ? __ldg(a.sa0_scale + row)
-                                                       : __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row);
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                if (hh) v1[j] *= sw * sxv[j];
-                                else v0[j] *= sw * sxv[j];
-                            }
-                        }
-                        if (MODE == kRouter) {
-                            float* dst = reinterpret_cast<float*>(a.out) + (size_t)it.ks * a.T * a.out_ld + row;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int col = g * 16 + j;
-                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_ld] = hh ? v1[j] : v0[j];
-                            }
-                        } else if (it.shared) {
-                            float* dst = reinterpret_cast<float*>(a.out_sh) + row;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int col = g * 16 + j;
-                                if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_sh_ld] = hh ? v1[j] : v0[j];
-                            }
-                        } else {
-                            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) + row;
+                    for (int gi = 0; gi < kMaxG; ++gi) {
+                        const int g = part + gi * (kEpiWarps / 4);
+                        if (g < nb) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 const int col = g * 16 + j;
                                 if (col < it.nrows)
-                                    dst[(size_t)(it.row0 + col) * a.out_ld] = __float2bfloat16_rn(hh ? v1[j] : v0[j]);
+                                    dst[(size_t)(it.row0 + col) * ld] = (uint16_t)(hp[gi][j >> 1] >> ((j & 1) * 16));
                             }
+                        }
+                    }
+                }
+                if (++acc == C::kNumAcc) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+                continue;
+            }
+            for (int g = part; g < nb; g += kEpiWarps / 4) {
+                float v0[16], v1[16];
+                tmem_ld16(tl + g * 16, v0);
+                if (NA == 2) tmem_ld16(tl + BN + g * 16, v1);
+                tmem_ld_wait();
+                // FP8 down: the token-row scales of this column group
+                float sxv[16];
+                if (MODE == kDownF8) {
+                    const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = g * 16 + j;
+                        sxv[j] = col < it.nrows ? __ldg(sbp + col) : 0.0f;
+                    }
+                }
+                // NA consecutive 128-row output blocks (down: rows m0.. and m0+128..)
+#pragma unroll
+                for (int hh = 0; hh < NA; ++hh) {
+                    const int row = mrow + hh * 128;
+                    if (row >= mlim) continue;
+                    if (MODE == kDownF8) {
+                        // dequantise: weight-row scale x intermediate-row scale
+                        const float sw = it.shared ? __ldg(a.sa0_scale + row)
+                                                   : __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (hh) v1[j] *= sw * sxv[j];
+                            else v0[j] *= sw * sxv[j];
+                        }
+                    }
+                    if (MODE == kRouter) {
+                        float* dst = reinterpret_cast<float*>(a.out) + (size_t)it.ks * a.T * a.out_ld + row;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = g * 16 + j;
+                            if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_ld] = hh ? v1[j] : v0[j];
+                        }
+                    } else if (it.shared) {
+                        float* dst = reinterpret_cast<float*>(a.out_sh) + row;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = g * 16 + j;
+                            if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_sh_ld] = hh ? v1[j] : v0[j];
+                        }
+                    } else {
+                        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) + row;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = g * 16 + j;
+                            if (col < it.nrows)
+                                dst[(size_t)(it.row0 + col) * a.out_ld] = __float2bfloat16_rn(hh ? v1[j] : v0[j]);
                         }
                     }
                 }
