@@ -44,6 +44,7 @@ struct Item {
     int nrows;   // valid B rows (<= BN)
     int kc0, kc1;
     int ks;      // router K split
+    int shared_a;  // the A tile is also read by other token chunks (keep it in L2 for them)
 };
 
 // Gate/up items carry the gate and the up tile of the same 128 rows; down items
@@ -106,6 +107,7 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Tabl
         it.nrows = min(BN, a.T - it.row0);
         it.kc0 = it.ks * a.kc_split;
         it.kc1 = min(a.kc_routed, it.kc0 + a.kc_split);
+        it.shared_a = chunks > 1;
         return it;
     }
     constexpr int RPI = Traits<MODE>::kRowsPerItem;
@@ -125,6 +127,7 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Tabl
         it.nrows = min(BN, a.T - it.row0);
         it.kc0 = 0;
         it.kc1 = a.kc_shared;
+        it.shared_a = chunks > 1;
         return it;
     }
     i -= n_sh_items;
@@ -147,6 +150,7 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs& a, const Tabl
     it.nrows = min(BN, cnt - c * BN);
     it.kc0 = 0;
     it.kc1 = a.kc_routed;
+    it.shared_a = chunks > 1;
     return it;
 }
 
@@ -252,7 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (warp == 0) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
+            // weights stream through L2 once (evict first) unless other token chunks of
+            // the same rows will read them too (evict normal, so those chunks hit)
+            const uint64_t pol_w1 = policy_evict_first();
+            const uint64_t pol_wn = policy_evict_normal();
             const uint64_t pol_x = policy_evict_last();
             uint32_t armed[STAGES];
             for (int s = 0; s < STAGES; ++s) armed[s] = 2;  // 2 = never armed
@@ -264,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const CUtensorMap* ma0 = it.shared ? &a.sa0 : &a.a0;
                 const CUtensorMap* ma1 = it.shared ? &a.sa1 : &a.a1;
                 const CUtensorMap* mb = it.shared ? a.sb : a.b;
+                const uint64_t pol_w = it.shared_a ? pol_wn : pol_w1;
                 // the chunk's rows rounded up to 16, one box per set bit of the 16-row count
                 const int nb = (it.nrows + 15) >> 4;
                 const uint32_t bytes = NA * kABytes + nb * 2048;
