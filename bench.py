@@ -499,15 +499,23 @@ def _oracle_tokens(w, toks, x, wr, b, experts, sh, threads):
         return list(ex.map(one, range(len(toks))))
 
 
-def cpu_baseline(w, dev, n_tok):
+def cpu_baseline(w, dev, n_tok, min_seconds=10.0):
+    """The oracle on the host cores: the first n_tok tokens of the batch, in
+    passes until at least min_seconds of wall time (bounded to 64 passes)."""
     threads = max(1, min(os.cpu_count() or 1, n_tok))
     toks, x, wr, b, experts, sh = _oracle_sample_inputs(w, n_tok, dev)
+    passes = 0
     t = time.perf_counter()
-    _oracle_tokens(w, toks, x, wr, b, experts, sh, threads)
-    dt = time.perf_counter() - t
-    return {"value": round(len(toks) / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+    while True:
+        _oracle_tokens(w, toks, x, wr, b, experts, sh, threads)
+        passes += 1
+        dt = time.perf_counter() - t
+        if dt >= min_seconds or passes >= 64:
+            break
+    return {"value": round(passes * len(toks) / dt, 3), "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"full layer output (router, top-{w.top_k}, {w.top_k} expert FFNs, shared, combine) of the "
-                      f"first {len(toks)} tokens of the {w.name} batch, fp64 C oracle, one token per thread",
+                      f"first {len(toks)} tokens of the {w.name} batch, {passes} passes, fp64 C oracle, one token "
+                      f"per thread",
             "seconds": round(dt, 3)}
 
 
