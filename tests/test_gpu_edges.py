@@ -99,3 +99,36 @@ def test_out_of_range_ids_through_dispatch_are_flagged_and_isolated():
     assert np.array_equal(perm.cpu().numpy(), perm_o)
     # the bad assignments sit after every valid slot, in the invalid bucket
     assert off_o[S] == n - 2 and set(perm_o[n - 2:]) == {2 * k + 0, 9 * k + 1}
+
+
+FP8_CASES = {k_: v for k_, v in CASES.items() if v.hidden % 16 == 0 and v.inter % 16 == 0
+             and (v.n_shared * v.inter_shared) % 16 == 0}
+
+
+@pytest.mark.parametrize("mode", [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL])
+@pytest.mark.parametrize("name", sorted(FP8_CASES))
+def test_fp8_edge_case_forward_matches_fp8_oracle(name, mode):
+    w = FP8_CASES[name]
+    T, H = w.tokens, w.hidden
+    x, wr = mi.hidden_states(w), mi.router_weight(w)
+    wg, wu, wd = mi.stacked_expert_weights(w)
+    if w.n_shared:
+        sg, su, sd = mi.stacked_shared_weights(w)
+    else:
+        sg = su = sd = None
+    q = oracle.quantize_layer_fp8(w, wg, wu, wd, sg, su, sd)
+    ref = oracle.moe_forward_fp8(w, x, wr, None, None, q)
+    d = {k_: torch.from_numpy(np.ascontiguousarray(v)).to(DEV) for k_, v in q.items()}
+    if not w.n_shared:
+        for k_ in ("qsg", "ssg", "qsu", "ssu", "qsd", "ssd"):
+            d[k_] = None
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(16, m.moe_workspace_size_fp8(w, T)), dtype=torch.uint8, device=DEV)
+    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), None, None, d["qg"], d["sg"], d["qu"], d["su"], d["qd"], d["sd"],
+                      d["qsg"], d["ssg"], d["qsu"], d["ssu"], d["qsd"], d["ssd"], out, topk_idx_out=idx, mode=mode,
+                      ws=ws)
+    assert m.moe_check_status() == 0, m.last_error()
+    lo = oracle.router_logits(w, x, wr, None)
+    sure = check_topk(idx.cpu().numpy(), ref["idx"], lo, w.top_k)
+    assert_close(to_np(out)[sure], ref["out"][sure], what=f"{name} fp8")
