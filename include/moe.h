@@ -31,7 +31,7 @@
  *     wait that expired) set a device status word instead of faulting;
  *     moe_check_status() synchronises the stream, reads and clears it.
  *   - T = 0 is valid and enqueues nothing.
- *   - Calls of at most 4096 token-expert assignments (T*k) launch their
+ *   - Calls of at most 8192 token-expert assignments (T*k) launch their
  *     kernels with programmatic dependent launch: a kernel may be scheduled
  *     while its predecessor in the stream finishes and waits for it before
  *     touching memory, so results and memory order are those of plain stream
