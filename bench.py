@@ -53,6 +53,21 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def max_over_ranks(value: float, device, world: int) -> float:
+    """The largest value over the ranks of the job (a step's time is its slowest
+    rank's); the value itself on one rank."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in ("grouped_gemm.cu", "common.cuh", "kernels.h"):
@@ -304,10 +319,7 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop() if rank == 0 else None
     elapsed_ms = t0.elapsed_time(t1)
     gu_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     rc = m.moe_check_status(stream)
     if rc != 0:
         raise RuntimeError("device status after timing: " + m.last_error())
@@ -370,11 +382,7 @@ def run_ours(args, rank, world, local_rank):
     e1 = torch.cuda.Event(enable_timing=True)
     e2e_run(args.steps, e0, e1)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev, world)
     if m.moe_check_status(stream) != 0:
         raise RuntimeError("device status after e2e: " + m.last_error())
 
@@ -386,10 +394,9 @@ def run_ours(args, rank, world, local_rank):
     ms_step = elapsed_ms / args.steps
     t_roof_ms = max(bf["bytes"] / (hbm * 1e9), bf["flops"] / (tf_sus * 1e12)) * 1e3
     achieved = bf["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
-    tokens = T * world
     res = {
         "metric": METRIC,
-        "value": round(tokens / (ms_step * 1e-3), 1),
+        "value": round(job_tokens_per_s(T, world, ms_step), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -431,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": src + " (hbm_gbs, copy bandwidth)",
         },
         "e2e": {
-            "value": round(tokens / (e2e_ms / args.steps * 1e-3), 1),
+            "value": round(job_tokens_per_s(T, world, e2e_ms / args.steps), 1),
             "unit": "tokens/s",
             "h2d_bytes_per_step": T * H * 2,
             "d2h_bytes_per_step": T * H * 2,
