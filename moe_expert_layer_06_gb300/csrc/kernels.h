@@ -100,7 +100,17 @@ struct GemmArgs {
 // for 4 pipeline stages (128 KB of weights in flight per SM).
 constexpr int kPrefillBN = 160;
 
-// Launch the grouped GEMM for `mode` with token chunk bn (32 or kPrefillBN).
+// Token chunk of the E4M3 expert GEMMs for 32 < T <= kMidMaxTokens: 128 rows
+// leave TMEM room for two accumulators (2 x 2 x 128 columns), so the next
+// item's MMAs start while the epilogue drains the last one.  An E4M3 item
+// streams half the bytes of a bf16 item, so the hand-off is a larger share of
+// it (measured on one GB300: redundant T=1024 -1.6%, skewed T=256 -0.8%; bf16
+// and T=4096 are faster with 160).
+constexpr int kMidBN = 128;
+constexpr int kMidMaxTokens = 1024;
+
+// Launch the grouped GEMM for `mode` with token chunk bn (32, kPrefillBN, or
+// kMidBN for the E4M3 modes).
 cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, cudaStream_t stream);
 int gemm_max_slots();
 

@@ -185,10 +185,11 @@ static int check_shape(const moe_shape_t* s, int T) {
 
 static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-static int ffn_bn(int T, int mode) {
+static int ffn_bn(int T, int mode, bool fp8) {
     if (mode == MOE_FFN_DECODE) return 32;
     if (mode == MOE_FFN_PREFILL) return kPrefillBN;
-    return T <= 32 ? 32 : kPrefillBN;
+    if (T <= 32) return 32;
+    return (fp8 && T <= kMidMaxTokens) ? kMidBN : kPrefillBN;
 }
 
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -334,7 +335,7 @@ static int gate_up_impl(const moe_shape_t* s, int T, const void* x, const void* 
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode);
+    const int bn = ffn_bn(T, mode, false);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_gate, s->n_slots, s->inter, s->hidden))) return rc;
@@ -395,7 +396,7 @@ static int gate_up_fp8_impl(const moe_shape_t* s, int T, const void* x8, const f
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode);
+    const int bn = ffn_bn(T, mode, true);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights_f8(&g.a0, qg, s->n_slots, s->inter, s->hidden))) return rc;
@@ -452,7 +453,7 @@ static int down_impl(const moe_shape_t* s, int T, const void* h_disp, const void
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode);
+    const int bn = ffn_bn(T, mode, false);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_down, s->n_slots, s->hidden, s->inter))) return rc;
@@ -509,7 +510,7 @@ static int down_fp8_impl(const moe_shape_t* s, int T, const void* h8, const floa
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode);
+    const int bn = ffn_bn(T, mode, true);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights_f8(&g.a0, qd, s->n_slots, s->hidden, s->inter))) return rc;

@@ -105,7 +105,7 @@ FP8_CASES = {k_: v for k_, v in CASES.items() if v.hidden % 16 == 0 and v.inter 
              and (v.n_shared * v.inter_shared) % 16 == 0}
 
 
-@pytest.mark.parametrize("mode", [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL])
+@pytest.mark.parametrize("mode", [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL, m.MOE_FFN_AUTO])
 @pytest.mark.parametrize("name", sorted(FP8_CASES))
 def test_fp8_edge_case_forward_matches_fp8_oracle(name, mode):
     w = FP8_CASES[name]

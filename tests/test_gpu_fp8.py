@@ -23,6 +23,11 @@ MID8 = mi.WORKLOADS["tiny"].with_(name="mid8", tokens=100, hidden=608, inter=336
                                   n_shared=2, inter_shared=200, n_slots=16, n_blocks=4)
 REP8 = mi.WORKLOADS["tiny"].with_(name="rep8", tokens=64, hidden=128, inter=64, n_experts=8, top_k=2,
                                   n_shared=1, inter_shared=64, n_slots=12, n_blocks=4)
+# 1040 assignments over 8 experts (~130 rows each): in the automatic mode most
+# experts take a full 128-row chunk and a ragged second one
+WIDE8 = mi.WORKLOADS["tiny"].with_(name="wide8", tokens=520, hidden=256, inter=128, n_experts=8, top_k=2,
+                                   n_shared=1, inter_shared=128, n_slots=8, n_blocks=4)
+MODES = [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL, m.MOE_FFN_AUTO]
 
 
 def _u8(a):
@@ -118,13 +123,13 @@ def test_shared_down_matrix_quantised_on_the_device_is_bit_exact():
     assert np.array_equal(codes.cpu().numpy(), c_o) and np.array_equal(scale.cpu().numpy(), s_o)
 
 
-@pytest.mark.parametrize("mode", [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL])
-@pytest.mark.parametrize("name", ["tiny", "mid8"])
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("name", ["tiny", "mid8", "wide8"])
 def test_fp8_intermediate_and_down_stage(name, mode):
     """Gate/up on the GPU, then the stage under test on the GPU's own h: the
     row quantiser (bit-exact against the oracle on the same bf16 h) and the
     FP8 down GEMM (against the oracle's down row on the same codes)."""
-    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8}[name]
+    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "wide8": WIDE8}[name]
     T, k, S, H, I = w.tokens, w.top_k, w.n_slots, w.hidden, w.inter
     Ks = w.n_shared * w.inter_shared
     q = _quantised_weights(w)
@@ -201,10 +206,10 @@ def test_fp8_dispatch_is_bit_exact(name):
     assert g["xd8"].numel() == T * k * H  # one byte per element: half the bf16 dispatch buffer
 
 
-@pytest.mark.parametrize("mode", [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL])
-@pytest.mark.parametrize("name", ["tiny", "mid8", "rep8"])
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("name", ["tiny", "mid8", "rep8", "wide8"])
 def test_fp8_layer_matches_fp8_oracle(name, mode):
-    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "rep8": REP8}[name]
+    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "rep8": REP8, "wide8": WIDE8}[name]
     rep = None
     if w.n_slots > w.n_experts:
         rep = oracle.plan_replicas(w, np.arange(w.n_experts)[::-1].copy(), w.n_slots - w.n_experts)
@@ -229,9 +234,12 @@ def test_fp8_layer_matches_fp8_oracle(name, mode):
 _EXPERTS = {}
 
 
-def test_fp8_layer_full_decode_shape_sampled_tokens():
+@pytest.fixture(scope="module")
+def fp8_dsv3():
+    """Every DeepSeek-V3-shaped expert and shared matrix quantised on the device
+    (the quantiser itself is pinned bit-exact above)."""
     w = mi.WORKLOADS["decode_t32"]
-    T, H, k = w.tokens, w.hidden, w.top_k
+    H = w.hidden
 
     def quant(t):
         q = torch.empty(t.shape, dtype=torch.uint8, device=DEV)
@@ -239,25 +247,44 @@ def test_fp8_layer_full_decode_shape_sampled_tokens():
         m.moe_quantize_rows_fp8(t.view(-1, t.shape[-1]), q, sc)
         return q, sc
 
+    d = {}
     wg, wu, wd = mi.stacked_expert_weights(w, device=DEV)
-    (qg, s_g), (qu, s_u), (qd, s_d) = quant(wg), quant(wu), quant(wd)
+    (d["qg"], d["sg"]), (d["qu"], d["su"]), (d["qd"], d["sd"]) = quant(wg), quant(wu), quant(wd)
     del wg, wu, wd
     sg, su, sd = mi.stacked_shared_weights(w, device=DEV)
-    (qsg, s_sg), (qsu, s_su) = quant(sg), quant(su)
-    qsd, s_sd = quant(sd.permute(1, 0, 2).reshape(H, -1).contiguous())
+    (d["qsg"], d["ssg"]), (d["qsu"], d["ssu"]) = quant(sg), quant(su)
+    d["qsd"], d["ssd"] = quant(sd.permute(1, 0, 2).reshape(H, -1).contiguous())
+    del sg, su, sd
+    torch.cuda.empty_cache()
+    return d
+
+
+# T = 32 runs the 32-row chunk, the skewed T = 256 batch the 128-row chunk of the
+# automatic mode (hot experts hold more than one chunk)
+@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew"])
+def test_fp8_layer_full_shape_sampled_tokens(name, fp8_dsv3):
+    w = mi.WORKLOADS[name]
+    T, H, k = w.tokens, w.hidden, w.top_k
+    d = fp8_dsv3
     x = mi.hidden_states(w)
     wr = mi.router_weight(w)
+    b = mi.router_bias(w)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
     tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
     ws = torch.empty(m.moe_workspace_size_fp8(w, T), dtype=torch.uint8, device=DEV)
-    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), None, None, qg, s_g, qu, s_u, qd, s_d, qsg, s_sg, qsu, s_su, qsd,
-                      s_sd, out, topk_idx_out=idx, topk_w_out=tw, ws=ws)
+    bd = torch.from_numpy(b).to(DEV) if b is not None else None
+    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), bd, None, d["qg"], d["sg"],
+                      d["qu"], d["su"], d["qd"], d["sd"], d["qsg"], d["ssg"], d["qsu"], d["ssu"], d["qsd"], d["ssd"],
+                      out, topk_idx_out=idx, topk_w_out=tw, ws=ws)
     assert m.moe_check_status() == 0, m.last_error()
-    lo = parallel_router_logits(w, x, wr, None)
+    lo = parallel_router_logits(w, x, wr, b)
     idx_o, wt_o = oracle.topk_softmax(lo, k)
     sure = check_topk(idx.cpu().numpy(), idx_o, lo, k)
-    toks = [t for t in (0, 13, 31) if sure[t]]
+    if name == "decode_t256_skew":
+        assert np.bincount(idx_o.ravel(), minlength=w.n_experts).max() > 128  # a two-chunk expert is present
+    toks = [t for t in (0, T // 3, (2 * T) // 3 + 1, T - 1) if sure[t]][:3]
+    assert toks
     qx, sx = oracle.quantize_rows_e4m3(x)
     sgc, suc, sdc = mi.stacked_shared_weights(w)
     qsh = {}
@@ -275,4 +302,4 @@ def test_fp8_layer_full_decode_shape_sampled_tokens():
         ysh = oracle.shared_row_fp8(w, qx[t], sx[t], qsh)
         ref = oracle.combine(w.with_(tokens=1), 1, np.stack(ys), np.arange(k, dtype=np.int32), wt_o[t:t + 1],
                              ysh[None, :])
-        assert_close(to_np(out)[t:t + 1], ref, what=f"fp8 decode token {t}")
+        assert_close(to_np(out)[t:t + 1], ref, what=f"fp8 {name} token {t}")
