@@ -70,9 +70,10 @@ extern "C" {
 
 /* Expert FFN kernel variant: token chunk of 32 rows (decode: weights streamed
  * once per 32 rows of an expert) or 160 rows (prefill).  AUTO picks 32 when
- * T <= 32 and 160 above, except the E4M3 calls (*_fp8) with T <= 1024, which
- * take a 128-row chunk with double-buffered accumulators.  Results are
- * identical up to fp32 summation order. */
+ * T <= 32 and 160 above, except the E4M3 down projection (moe_expert_down_fp8,
+ * and inside moe_forward_fp8) with T <= 1024, which takes a 128-row chunk with
+ * double-buffered accumulators.  Results are identical up to fp32 summation
+ * order. */
 #define MOE_FFN_AUTO 0
 #define MOE_FFN_DECODE 1
 #define MOE_FFN_PREFILL 2

@@ -577,11 +577,7 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, c
             case kRouter: return launch_one<kRouter, 32, 8>(args, grid, stream);
         }
     } else if (bn == kMidBN) {
-        switch (mode) {
-            case kGateUpF8: return launch_one<kGateUpF8, kMidBN, 4>(args, grid, stream);
-            case kDownF8: return launch_one<kDownF8, kMidBN, 4>(args, grid, stream);
-            default: return cudaErrorInvalidValue;
-        }
+        if (mode == kDownF8) return launch_one<kDownF8, kMidBN, 4>(args, grid, stream);
     } else if (bn == kPrefillBN) {
         switch (mode) {
             case kGateUpF8: return launch_one<kGateUpF8, kPrefillBN, 4>(args, grid, stream);

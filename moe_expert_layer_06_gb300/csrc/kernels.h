@@ -100,17 +100,18 @@ struct GemmArgs {
 // for 4 pipeline stages (128 KB of weights in flight per SM).
 constexpr int kPrefillBN = 160;
 
-// Token chunk of the E4M3 expert GEMMs for 32 < T <= kMidMaxTokens: 128 rows
-// leave TMEM room for two accumulators (2 x 2 x 128 columns), so the next
-// item's MMAs start while the epilogue drains the last one.  An E4M3 item
-// streams half the bytes of a bf16 item, so the hand-off is a larger share of
-// it (measured on one GB300: redundant T=1024 -1.6%, skewed T=256 -0.8%; bf16
-// and T=4096 are faster with 160).
+// Token chunk of the E4M3 down GEMM for 32 < T <= kMidMaxTokens.  An E4M3 down
+// item runs only ceil(I/128) K chunks (16 at I = 2048), so handing its
+// accumulator to the epilogue is a large share of it; 128 rows leave TMEM room
+// for two accumulators (2 x 2 x 128 columns), and the next item's MMAs start
+// while the epilogue drains the last one (measured on one GB300: redundant
+// T=1024 -2.1%, skewed T=256 -2.2%).  The E4M3 gate/up (56 K chunks an item),
+// the bf16 GEMMs and T=4096 are as fast or faster with 160.
 constexpr int kMidBN = 128;
 constexpr int kMidMaxTokens = 1024;
 
 // Launch the grouped GEMM for `mode` with token chunk bn (32, kPrefillBN, or
-// kMidBN for the E4M3 modes).
+// kMidBN for the E4M3 down).
 cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, cudaStream_t stream);
 int gemm_max_slots();
 

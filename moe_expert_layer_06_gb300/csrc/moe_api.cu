@@ -185,11 +185,12 @@ static int check_shape(const moe_shape_t* s, int T) {
 
 static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-static int ffn_bn(int T, int mode, bool fp8) {
+// mid: the E4M3 down GEMM, which takes kMidBN rows for mid-size batches
+static int ffn_bn(int T, int mode, bool mid) {
     if (mode == MOE_FFN_DECODE) return 32;
     if (mode == MOE_FFN_PREFILL) return kPrefillBN;
     if (T <= 32) return 32;
-    return (fp8 && T <= kMidMaxTokens) ? kMidBN : kPrefillBN;
+    return (mid && T <= kMidMaxTokens) ? kMidBN : kPrefillBN;
 }
 
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -396,7 +397,7 @@ static int gate_up_fp8_impl(const moe_shape_t* s, int T, const void* x8, const f
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode, true);
+    const int bn = ffn_bn(T, mode, false);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights_f8(&g.a0, qg, s->n_slots, s->inter, s->hidden))) return rc;

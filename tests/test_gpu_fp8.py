@@ -23,8 +23,8 @@ MID8 = mi.WORKLOADS["tiny"].with_(name="mid8", tokens=100, hidden=608, inter=336
                                   n_shared=2, inter_shared=200, n_slots=16, n_blocks=4)
 REP8 = mi.WORKLOADS["tiny"].with_(name="rep8", tokens=64, hidden=128, inter=64, n_experts=8, top_k=2,
                                   n_shared=1, inter_shared=64, n_slots=12, n_blocks=4)
-# 1040 assignments over 8 experts (~130 rows each): in the automatic mode most
-# experts take a full 128-row chunk and a ragged second one
+# 1040 assignments over 8 experts (~130 rows each): in the automatic mode the
+# down projection of most experts takes a full 128-row chunk and a ragged second one
 WIDE8 = mi.WORKLOADS["tiny"].with_(name="wide8", tokens=520, hidden=256, inter=128, n_experts=8, top_k=2,
                                    n_shared=1, inter_shared=128, n_slots=8, n_blocks=4)
 MODES = [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL, m.MOE_FFN_AUTO]
@@ -259,8 +259,8 @@ def fp8_dsv3():
     return d
 
 
-# T = 32 runs the 32-row chunk, the skewed T = 256 batch the 128-row chunk of the
-# automatic mode (hot experts hold more than one chunk)
+# T = 32 runs the 32-row chunk, the skewed T = 256 batch the 160-row gate/up and
+# the 128-row down chunk of the automatic mode (hot experts hold more than one)
 @pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew"])
 def test_fp8_layer_full_shape_sampled_tokens(name, fp8_dsv3):
     w = mi.WORKLOADS[name]
