@@ -254,6 +254,7 @@ def run_ours(args, rank, world, local_rank):
     rws = torch.empty(max(16, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    ffn_mode = {"auto": m.MOE_FFN_AUTO, "decode": m.MOE_FFN_DECODE, "prefill": m.MOE_FFN_PREFILL}[args.ffn_mode]
     groups = None
     if args.route_groups:
         groups = tuple(int(v) for v in args.route_groups.split(":"))
@@ -272,18 +273,18 @@ def run_ours(args, rank, world, local_rank):
             ev[0].record(stream)
         if fp8:
             m.moe_expert_gate_up_fp8(w, T, x8, xs8, x_disp8, xds8, offsets, qg, s_g, qu, s_u, qsg, s_sg, qsu, s_su,
-                                     h, hs)
+                                     h, hs, mode=ffn_mode)
         else:
-            m.moe_expert_gate_up(w, T, x, x_disp, offsets, wg, wu, sg, su, h, hs)
+            m.moe_expert_gate_up(w, T, x, x_disp, offsets, wg, wu, sg, su, h, hs, mode=ffn_mode)
         if ev is not None:
             ev[1].record(stream)
         if fp8:
             m.moe_quantize_rows_fp8(h, h8, h8s)
             if w.n_shared:
                 m.moe_quantize_rows_fp8(hs, hs8, hs8s)
-            m.moe_expert_down_fp8(w, T, h8, h8s, hs8, hs8s, offsets, qd, s_d, qsd, s_sd, y, ysh)
+            m.moe_expert_down_fp8(w, T, h8, h8s, hs8, hs8s, offsets, qd, s_d, qsd, s_sd, y, ysh, mode=ffn_mode)
         else:
-            m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh)
+            m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh, mode=ffn_mode)
         m.moe_combine(w, T, y, inv, tw, ysh, out)
 
     # router GEMM + top-k, index pass (three launches in chunks for large batches), scatter
@@ -345,9 +346,9 @@ def run_ours(args, rank, world, local_rank):
             ob.copy_(out)
         elif fp8:
             m.moe_forward_fp8(w, T, xb, wr, bias, repd, qg, s_g, qu, s_u, qd, s_d, qsg, s_sg, qsu, s_su, qsd, s_sd,
-                              ob, ws=ws)
+                              ob, mode=ffn_mode, ws=ws)
         else:
-            m.moe_forward(w, T, xb, wr, bias, repd, wg, wu, wd, sg, su, sd, ob, ws=ws)
+            m.moe_forward(w, T, xb, wr, bias, repd, wg, wu, wd, sg, su, sd, ob, mode=ffn_mode, ws=ws)
 
     def e2e_run(n, e_begin=None, e_end=None):
         with torch.cuda.stream(copy_stream):
@@ -410,7 +411,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {
             "workload": w.name, "description": w.description, "tokens": T, "hidden": H, "inter": I,
             "n_experts": E, "top_k": k, "n_shared": w.n_shared, "n_slots": S,
-            "touched_slots": bf["touched"],
+            "touched_slots": bf["touched"], "ffn_mode": args.ffn_mode,
             "l2": "inputs larger than L2: each step streams %.1f GB of touched expert weights" % (bf["bytes"] / 1e9),
             "parallelism": "replica x%d (independent layer per GPU)" % world,
             "routing": ("group-limited: %d groups, keep %d" % groups) if groups else "top-%d of all experts" % k,
@@ -665,6 +666,8 @@ def main():
     ap.add_argument("--route-groups", default="", help="G:Gk group-limited routing (timed region only)")
     ap.add_argument("--eplb", action="store_true", help="time the online EPLB loop instead (own JSON line)")
     ap.add_argument("--fp8", action="store_true", help="E4M3 expert weights and dispatch payload")
+    ap.add_argument("--ffn-mode", default="auto", choices=["auto", "decode", "prefill"],
+                    help="expert GEMM token chunk: automatic, 32 rows, or 160 rows")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -71,9 +71,9 @@ extern "C" {
 /* Expert FFN kernel variant: token chunk of 32 rows (decode: weights streamed
  * once per 32 rows of an expert) or 160 rows (prefill).  AUTO picks 32 when
  * T <= 32 and 160 above, except the E4M3 down projection (moe_expert_down_fp8,
- * and inside moe_forward_fp8) with T <= 1024, which takes a 128-row chunk with
- * double-buffered accumulators.  Results are identical up to fp32 summation
- * order. */
+ * and inside moe_forward_fp8) when the batch averages at most 32 rows per slot
+ * (T*k <= 32*S), which takes a 128-row chunk with double-buffered
+ * accumulators.  Results are identical up to fp32 summation order. */
 #define MOE_FFN_AUTO 0
 #define MOE_FFN_DECODE 1
 #define MOE_FFN_PREFILL 2

@@ -100,15 +100,17 @@ struct GemmArgs {
 // for 4 pipeline stages (128 KB of weights in flight per SM).
 constexpr int kPrefillBN = 160;
 
-// Token chunk of the E4M3 down GEMM for 32 < T <= kMidMaxTokens.  An E4M3 down
-// item runs only ceil(I/128) K chunks (16 at I = 2048), so handing its
-// accumulator to the epilogue is a large share of it; 128 rows leave TMEM room
-// for two accumulators (2 x 2 x 128 columns), and the next item's MMAs start
-// while the epilogue drains the last one (measured on one GB300: redundant
-// T=1024 -2.1%, skewed T=256 -2.2%).  The E4M3 gate/up (56 K chunks an item),
-// the bf16 GEMMs and T=4096 are as fast or faster with 160.
+// Token chunk of the E4M3 down GEMM when T > 32 and the batch averages at most
+// kMidMaxRowsPerSlot rows per slot (T*k <= kMidMaxRowsPerSlot*S; T <= 1024 at
+// 256 experts, top-8).  An E4M3 down item runs only ceil(I/128) K chunks (16 at
+// I = 2048), so handing its accumulator to the epilogue is a large share of it;
+// 128 rows leave TMEM room for two accumulators (2 x 2 x 128 columns), and the
+// next item's MMAs start while the epilogue drains the last one (measured on
+// one GB300: redundant T=1024 -1.9%, skewed T=256 -2.1%).  With ~128 rows per
+// expert, 128-row chunks split half the experts in two and 160 is faster; so
+// are the E4M3 gate/up (56 K chunks an item) and the bf16 GEMMs.
 constexpr int kMidBN = 128;
-constexpr int kMidMaxTokens = 1024;
+constexpr int kMidMaxRowsPerSlot = 32;
 
 // Launch the grouped GEMM for `mode` with token chunk bn (32, kPrefillBN, or
 // kMidBN for the E4M3 down).

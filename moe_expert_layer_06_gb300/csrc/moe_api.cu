@@ -185,12 +185,13 @@ static int check_shape(const moe_shape_t* s, int T) {
 
 static inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// mid: the E4M3 down GEMM, which takes kMidBN rows for mid-size batches
-static int ffn_bn(int T, int mode, bool mid) {
+// mid: the E4M3 down GEMM, which takes kMidBN rows when slots average few rows
+static int ffn_bn(const moe_shape_t* s, int T, int mode, bool mid) {
     if (mode == MOE_FFN_DECODE) return 32;
     if (mode == MOE_FFN_PREFILL) return kPrefillBN;
     if (T <= 32) return 32;
-    return (mid && T <= kMidMaxTokens) ? kMidBN : kPrefillBN;
+    const bool few_rows = (long)T * s->top_k <= (long)kMidMaxRowsPerSlot * s->n_slots;
+    return (mid && few_rows) ? kMidBN : kPrefillBN;
 }
 
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -336,7 +337,7 @@ static int gate_up_impl(const moe_shape_t* s, int T, const void* x, const void* 
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode, false);
+    const int bn = ffn_bn(s, T, mode, false);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_gate, s->n_slots, s->inter, s->hidden))) return rc;
@@ -397,7 +398,7 @@ static int gate_up_fp8_impl(const moe_shape_t* s, int T, const void* x8, const f
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode, false);
+    const int bn = ffn_bn(s, T, mode, false);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights_f8(&g.a0, qg, s->n_slots, s->inter, s->hidden))) return rc;
@@ -454,7 +455,7 @@ static int down_impl(const moe_shape_t* s, int T, const void* h_disp, const void
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode, false);
+    const int bn = ffn_bn(s, T, mode, false);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_down, s->n_slots, s->hidden, s->inter))) return rc;
@@ -511,7 +512,7 @@ static int down_fp8_impl(const moe_shape_t* s, int T, const void* h8, const floa
     int rc = device_status(&st);
     if (rc) return rc;
     const int n = T * s->top_k;
-    const int bn = ffn_bn(T, mode, true);
+    const int bn = ffn_bn(s, T, mode, true);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights_f8(&g.a0, qd, s->n_slots, s->hidden, s->inter))) return rc;

@@ -217,6 +217,11 @@ WORKLOADS = {
                                  router_std=0.02, skew_alpha=0.0,
                                  description="profiling case: DeepSeek-V3 expert shapes, 32 experts, "
                                              "T=512 (128 rows per expert, as prefill T=4096)"),
+    "decode_t128_e32": Workload(name="decode_t128_e32", tokens=128, hidden=7168, inter=2048, n_experts=32,
+                                top_k=8, n_shared=2, inter_shared=2048, n_slots=32, n_blocks=8,
+                                router_std=0.02, skew_alpha=0.0,
+                                description="profiling case: DeepSeek-V3 expert shapes, 32 experts, "
+                                            "T=128 (32 rows per expert, as T=1024 over 256 experts)"),
 }
 
 # the skewed decode workload whose histogram chooses the 8 replicated experts

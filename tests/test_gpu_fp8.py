@@ -23,10 +23,11 @@ MID8 = mi.WORKLOADS["tiny"].with_(name="mid8", tokens=100, hidden=608, inter=336
                                   n_shared=2, inter_shared=200, n_slots=16, n_blocks=4)
 REP8 = mi.WORKLOADS["tiny"].with_(name="rep8", tokens=64, hidden=128, inter=64, n_experts=8, top_k=2,
                                   n_shared=1, inter_shared=64, n_slots=12, n_blocks=4)
-# 1040 assignments over 8 experts (~130 rows each): in the automatic mode the
-# down projection of most experts takes a full 128-row chunk and a ragged second one
-WIDE8 = mi.WORKLOADS["tiny"].with_(name="wide8", tokens=520, hidden=256, inter=128, n_experts=8, top_k=2,
-                                   n_shared=1, inter_shared=128, n_slots=8, n_blocks=4)
+# 800 assignments over 32 experts (25 rows a slot on average, so the automatic
+# mode gives the E4M3 down 128-row chunks), skewed so that two experts hold
+# ~400 rows each: several full chunks and a ragged one, and many empty slots
+SKEW8 = mi.WORKLOADS["tiny"].with_(name="skew8", tokens=400, hidden=256, inter=128, n_experts=32, top_k=2,
+                                   n_shared=1, inter_shared=128, n_slots=32, n_blocks=4, skew_alpha=1.5)
 MODES = [m.MOE_FFN_DECODE, m.MOE_FFN_PREFILL, m.MOE_FFN_AUTO]
 
 
@@ -124,12 +125,12 @@ def test_shared_down_matrix_quantised_on_the_device_is_bit_exact():
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("name", ["tiny", "mid8", "wide8"])
+@pytest.mark.parametrize("name", ["tiny", "mid8", "skew8"])
 def test_fp8_intermediate_and_down_stage(name, mode):
     """Gate/up on the GPU, then the stage under test on the GPU's own h: the
     row quantiser (bit-exact against the oracle on the same bf16 h) and the
     FP8 down GEMM (against the oracle's down row on the same codes)."""
-    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "wide8": WIDE8}[name]
+    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "skew8": SKEW8}[name]
     T, k, S, H, I = w.tokens, w.top_k, w.n_slots, w.hidden, w.inter
     Ks = w.n_shared * w.inter_shared
     q = _quantised_weights(w)
@@ -207,23 +208,25 @@ def test_fp8_dispatch_is_bit_exact(name):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("name", ["tiny", "mid8", "rep8", "wide8"])
+@pytest.mark.parametrize("name", ["tiny", "mid8", "rep8", "skew8"])
 def test_fp8_layer_matches_fp8_oracle(name, mode):
-    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "rep8": REP8, "wide8": WIDE8}[name]
+    w = {"tiny": mi.WORKLOADS["tiny"], "mid8": MID8, "rep8": REP8, "skew8": SKEW8}[name]
     rep = None
     if w.n_slots > w.n_experts:
         rep = oracle.plan_replicas(w, np.arange(w.n_experts)[::-1].copy(), w.n_slots - w.n_experts)
     T, H = w.tokens, w.hidden
     x, wr = mi.hidden_states(w), mi.router_weight(w)
     q = _quantised_weights(w, rep)
-    ref = oracle.moe_forward_fp8(w, x, wr, None, rep, q)
-    lo = oracle.router_logits(w, x, wr, None)
+    b = mi.router_bias(w)
+    ref = oracle.moe_forward_fp8(w, x, wr, b, rep, q)
+    lo = oracle.router_logits(w, x, wr, b)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     idx = torch.empty((T, w.top_k), dtype=torch.int32, device=DEV)
     ws = torch.empty(m.moe_workspace_size_fp8(w, T), dtype=torch.uint8, device=DEV)
     repd = torch.from_numpy(rep).to(DEV) if rep is not None else None
     d = _dev(q)
-    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), None, repd, d["qg"], d["sg"], d["qu"], d["su"], d["qd"], d["sd"],
+    bd = torch.from_numpy(b).to(DEV) if b is not None else None
+    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), bd, repd, d["qg"], d["sg"], d["qu"], d["su"], d["qd"], d["sd"],
                       d["qsg"], d["ssg"], d["qsu"], d["ssu"], d["qsd"], d["ssd"], out, topk_idx_out=idx, mode=mode,
                       ws=ws)
     assert m.moe_check_status() == 0, m.last_error()
