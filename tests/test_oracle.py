@@ -248,6 +248,11 @@ def test_payload_bytes_match_pages():
     assert wr.n_slots // wr.n_blocks == rows["slots_per_rank_redundant"][0]
     assert (wr.n_slots - wr.n_experts) * per_expert == rows["redundant_bytes_fp16"][0]
     assert w.n_experts // w.n_blocks == rows["experts_per_rank"][0]
+    # the decode bottleneck arithmetic quoted as context for the roofline (H800, 50 ms TPOT)
+    assert 3350e9 * 0.050 * 0.5 == rows["tpot_bytes_h800"][0]
+    assert round(85 / 22) == rows["decode_batch_no_ep"][0]  # 3.9 rounds to 4
+    assert 8 * rows["decode_batch_no_ep"][0] == rows["decode_batch_ep8"][0]  # EP = 8 divides the weights by 8
+    assert abs(85 / (22 / 8) - rows["decode_batch_ep8"][0]) / rows["decode_batch_ep8"][0] < 0.04  # 30.9
 
 
 # ------------------------------------------------------------------ FFN and layer math
