@@ -628,3 +628,29 @@ def test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors():
     # and it stays close to the bf16 layer
     r16 = oracle.moe_forward(w, x, wr, None, None, wg, wu, wd, sg, su, sd)
     assert np.linalg.norm(r["out"] - r16["out"]) / np.linalg.norm(r16["out"]) < 0.1
+
+
+def test_skewed_batch_triggers_rebalancing_and_replicas_lower_the_block_imbalance():
+    """The load-balancing story of "专家并行（EP）" sections 6.1-6.3 on the skewed
+    workloads: the T = 256 batch's EP-block load ratio (max over mean) is past
+    the 1.2 trigger, and the replica plan drawn from its histogram lowers the
+    block imbalance of the T = 1024 batch (a hot expert's odd tokens go to its
+    replica in another block) without changing the number of assignments."""
+    src = mi.WORKLOADS[mi.REPLICA_PLAN_SOURCE]
+    lo = oracle.router_logits(src, mi.hidden_states(src), mi.router_weight(src), mi.router_bias(src))
+    idx, _ = oracle.topk_softmax(lo, src.top_k)
+    so, _ = oracle.slot_map(src, idx)
+    counts, blocks = oracle.histogram(src, so)
+    _, bl, _, ratio, trig = oracle.eplb_window(src, counts[None, :], 1, None, 1.2)
+    assert np.array_equal(bl, blocks)
+    assert ratio == pytest.approx(blocks.max() / blocks.mean(), rel=1e-12)
+    assert ratio > 1.2 and trig
+    w = mi.WORKLOADS["redundant_t1024"]
+    rep = oracle.plan_replicas(w, np.bincount(idx.ravel(), minlength=w.n_experts), mi.N_REPLICAS)
+    lo2 = oracle.router_logits(w, mi.hidden_states(w), mi.router_weight(w), mi.router_bias(w))
+    idx2, _ = oracle.topk_softmax(lo2, w.top_k)
+    plain = w.with_(n_slots=w.n_experts)
+    _, b_plain = oracle.histogram(plain, oracle.slot_map(plain, idx2)[0])
+    _, b_rep = oracle.histogram(w, oracle.slot_map(w, idx2, rep)[0])
+    assert b_plain.sum() == b_rep.sum() == w.tokens * w.top_k
+    assert b_rep.max() / b_rep.mean() < b_plain.max() / b_plain.mean()
