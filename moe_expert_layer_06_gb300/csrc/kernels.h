@@ -58,10 +58,11 @@ enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2, kGateUpF8 = 3, kDownF
 
 // One launch computes D = A * B^T for a list of work items.  A is a weight
 // tile of 128 output rows (the UMMA M operand), B is a chunk of up to BN
-// token rows (the UMMA N operand), K runs over 64-element chunks.  Every
-// operand is read by TMA through the tensor maps below (3-D, bf16, 128-byte
-// swizzle; weights box {64, 128, 1}; tokens box {64, 1, 16 << j}, so a chunk of
-// n 16-row groups is loaded exactly with one box per set bit of n).
+// token rows (the UMMA N operand), K runs over 128-byte chunks (64 bf16 or
+// 128 E4M3 elements).  Every operand is read by TMA through the tensor maps
+// below (3-D, 128-byte swizzle; weights box {128 B, 128, 1}; tokens box
+// {128 B, 1, 16 << j}, so a chunk of n 16-row groups is loaded exactly with one
+// box per set bit of n).
 struct GemmArgs {
     CUtensorMap a0;   // routed weights: gate [S,I,H] | down [S,H,I] | router [1,E,H]
     CUtensorMap a1;   // routed up weights [S,I,H] (gate/up only)
@@ -73,11 +74,12 @@ struct GemmArgs {
     int n_slots;
     int T;
     int m_routed;     // output rows per routed matrix: I | H | E
-    int kc_routed;    // 64-wide K chunks of a routed item
+    int kc_routed;    // K chunks (128 bytes each) of a routed item
     int n_shared;     // shared experts (0: none)
     int m_shared;     // output rows per shared matrix: I_sh | H
-    int kc_shared;    // K chunks of a shared item: ceil(H/64) | n_sh*ceil(I_sh/64)
-    int kc_per_sh;    // down: K chunks per shared expert, ceil(I_sh/64)
+    int kc_shared;    // K chunks of a shared item: ceil(H/64) | n_sh*ceil(I_sh/64) (E4M3: /128, one
+                      // concatenated shared down matrix)
+    int kc_per_sh;    // bf16 down: K chunks per shared expert, ceil(I_sh/64)
     int ksplit;       // router: number of K splits
     int kc_split;     // router: K chunks per split
     void* out;        // h_disp bf16 | y_disp bf16 | logit partials f32 [ksplit,T,E]
@@ -115,7 +117,7 @@ constexpr int kMidMaxRowsPerSlot = 32;
 // Launch the grouped GEMM for `mode` with token chunk bn (32, kPrefillBN, or
 // kMidBN for the E4M3 down).
 cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, cudaStream_t stream);
-int gemm_max_slots();
+int gemm_max_slots();  // slots the GEMM's shared-memory item table holds
 
 // ---------------------------------------------------------------- TMA tensor maps
 // 3-D bf16 tensor map, dims innermost first (elements), strides of dims 1,2 in bytes.
@@ -162,7 +164,7 @@ size_t index_workspace_bytes(int n, int n_slots);
 cudaError_t launch_index_chunked(const DispatchArgs& a, int32_t* hist, cudaStream_t stream);
 cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* perm, int n_rows, int k, int hidden,
                                 uint16_t* x_disp, cudaStream_t stream);
-int dispatch_max_slots();
+int dispatch_max_slots();  // slots the index pass's shared-memory histograms hold
 
 // ---------------------------------------------------------------- combine
 cudaError_t launch_combine(const uint16_t* y_disp, const int32_t* inv_perm, const float* topk_w,

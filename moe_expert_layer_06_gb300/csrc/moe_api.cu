@@ -164,8 +164,9 @@ static int check_shape(const moe_shape_t* s, int T) {
         return fail(MOE_ERR_INVALID_ARG, "hidden, inter and inter_shared must be multiples of 8");
     if (s->n_experts % s->n_blocks || s->n_slots % s->n_blocks || s->n_slots < s->n_experts)
         return fail(MOE_ERR_INVALID_ARG, "n_experts and n_slots must divide into n_blocks, n_slots >= n_experts");
-    if (s->n_experts > 1024) return fail(MOE_ERR_UNSUPPORTED, "n_experts %d > 1024", s->n_experts);
-    if (s->n_slots > 1024) return fail(MOE_ERR_UNSUPPORTED, "n_slots %d > 1024", s->n_slots);
+    const int max_slots = std::min(gemm_max_slots(), dispatch_max_slots());
+    if (s->n_experts > max_slots) return fail(MOE_ERR_UNSUPPORTED, "n_experts %d > %d", s->n_experts, max_slots);
+    if (s->n_slots > max_slots) return fail(MOE_ERR_UNSUPPORTED, "n_slots %d > %d", s->n_slots, max_slots);
     if ((int64_t)T * s->top_k > INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "T*k too large");
     return MOE_OK;
 }
