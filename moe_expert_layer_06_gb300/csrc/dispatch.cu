@@ -307,16 +307,12 @@ int dispatch_max_slots() { return kMaxSlots; }
 cudaError_t launch_index_pass(const DispatchArgs& a, cudaStream_t stream) {
     const int NS = a.S + 1;
     const size_t smem = (size_t)(NS + (NS + 1) + NS + 32 * NS) * sizeof(int);
-    static int configured_device = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<uint64_t> configured{0};
+    const cudaError_t e = configure_once(configured, [] {
+        return cudaFuncSetAttribute(index_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)((kMaxSlots + 1) * 35 + 8) * (int)sizeof(int));
+    });
     if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(index_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)((kMaxSlots + 1) * 35 + 8) * (int)sizeof(int));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
     return launch_pdl(index_pass_kernel, dim3(1), dim3(kIdxThreads), smem, stream, a);
 }
 
@@ -336,16 +332,12 @@ cudaError_t launch_index_chunked(const DispatchArgs& a, int32_t* hist, cudaStrea
     const int n_chunks = index_chunks(n);
     const int chunk = (n + n_chunks - 1) / n_chunks;
     const int NS = a.S + 1;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<uint64_t> configured{0};
+    cudaError_t e = configure_once(configured, [] {
+        return cudaFuncSetAttribute(index_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(kChunkWarps * (kMaxSlots + 1) * sizeof(int)));
+    });
     if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(index_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kChunkWarps * (kMaxSlots + 1) * sizeof(int)));
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
     e = launch_pdl(index_hist_kernel, dim3(n_chunks), dim3(kChunkThreads), NS * sizeof(int), stream, a, chunk, hist);
     if (e != cudaSuccess) return e;
     e = launch_pdl(index_scan_kernel, dim3(1), dim3(kIdxThreads), (2 * NS + 1) * sizeof(int), stream, a, n_chunks, hist);

@@ -550,15 +550,11 @@ template <int MODE, int BN, int STAGES>
 cudaError_t launch_one(const GemmArgs& args, int grid, cudaStream_t stream) {
     using C = Config<MODE, BN, STAGES>;
     auto kern = grouped_gemm_kernel<MODE, BN, STAGES>;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<uint64_t> configured{0};
+    const cudaError_t e = configure_once(configured, [&] {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    });
     if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
     return launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, args);
 }
 

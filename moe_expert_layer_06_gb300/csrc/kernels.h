@@ -7,6 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "moe.h"
@@ -46,6 +47,24 @@ inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, si
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Run `configure` (a kernel attribute such as its dynamic shared memory) the
+// first time the calling thread's device needs it, from any number of host
+// threads: `done` holds one bit per configured device (ordinals 0..63; others
+// configure on every call).  Concurrent first calls may both configure, which
+// is idempotent.
+template <typename F>
+inline cudaError_t configure_once(std::atomic<uint64_t>& done, F&& configure) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return configure();
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = configure();
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 // ---------------------------------------------------------------- grouped swap-AB GEMM (tcgen05)

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "moe.h"
@@ -36,10 +37,12 @@ static int cuda_fail(cudaError_t e, const char* what) {
 
 // ------------------------------------------------------------------ device status
 __device__ unsigned int g_status_word;
-static unsigned long long g_wait_limit_ns = 2000000000ull;
+// Shared by every host thread: the wait bound (set by moe_set_wait_limit_ns) and
+// per-device caches filled on first use (a racing first use fills the same value).
+static std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 static constexpr int kMaxDevices = 64;
-static unsigned int* g_status_ptr[kMaxDevices];
-static int g_num_sms[kMaxDevices];
+static std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+static std::atomic<int> g_num_sms[kMaxDevices];
 
 static int current_device(int* dev) {
     cudaError_t e = cudaGetDevice(dev);
@@ -52,25 +55,27 @@ static int device_status(DevStatus* st) {
     int dev;
     int rc = current_device(&dev);
     if (rc) return rc;
-    if (!g_status_ptr[dev]) {
+    unsigned int* word = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (!word) {
         void* p = nullptr;
         MOE_CUDA(cudaGetSymbolAddress(&p, g_status_word), "cudaGetSymbolAddress(status)");
-        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+        word = static_cast<unsigned int*>(p);
+        g_status_ptr[dev].store(word, std::memory_order_release);
     }
-    st->word = g_status_ptr[dev];
-    st->limit_ns = g_wait_limit_ns;
+    st->word = word;
+    st->limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     return MOE_OK;
 }
 
 int num_sms() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-    if (!g_num_sms[dev]) {
-        int n = 0;
+    int n = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        g_num_sms[dev] = n;
+        g_num_sms[dev].store(n, std::memory_order_relaxed);
     }
-    return g_num_sms[dev];
+    return n;
 }
 
 // ------------------------------------------------------------------ tensor maps
@@ -78,16 +83,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Looked up once (thread-safe static initialisation); null without a driver.
 static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static const EncodeTiledFn fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -681,7 +687,7 @@ int moe_abi_version(void) { return 1; }
 
 int moe_set_wait_limit_ns(uint64_t ns) {
     if (ns == 0) return fail(MOE_ERR_INVALID_ARG, "wait limit must be > 0");
-    g_wait_limit_ns = ns;
+    g_wait_limit_ns.store(ns, std::memory_order_relaxed);
     return MOE_OK;
 }
 
