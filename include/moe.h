@@ -31,6 +31,11 @@
  *     wait that expired) set a device status word instead of faulting;
  *     moe_check_status() synchronises the stream, reads and clears it.
  *   - T = 0 is valid and enqueues nothing.
+ *   - Any number of host threads may call concurrently, each on its own
+ *     stream and buffers: the library's per-device set-up is done once under
+ *     atomics, the error text is per thread, and the device status word is
+ *     shared (one thread's moe_check_status may report and clear another's
+ *     error).  moe_expert_ffn_noalloc calls must not overlap (one scratch).
  *   - Calls of at most 8192 token-expert assignments (T*k) launch their
  *     kernels with programmatic dependent launch: a kernel may be scheduled
  *     while its predecessor in the stream finishes and waits for it before
