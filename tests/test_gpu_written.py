@@ -3,8 +3,9 @@ staged calls and of the whole-layer calls is filled with a sentinel first
 (NaN for floating point, 0x7F for E4M3 codes, which the saturating quantiser
 never produces, an unlikely value for integers), so an element a kernel skips
 cannot pass by holding an earlier run's value.  Ragged shapes, the chunked
-index pass and all three kernel variants (32-, 128- and 160-row token
-chunks)."""
+index pass, all three kernel variants (32-, 128- and 160-row token chunks),
+both precisions, group-limited routing, the histogram-only call and the
+combined expert FFN."""
 import pytest
 import torch
 
@@ -130,5 +131,44 @@ def test_staged_fp8_calls_write_every_output_element(w, mode):
     m.moe_expert_down_fp8(w, T, o["h8"], o["h8s"], o["hs8"], o["hs8s"], o["offsets"], qd, s_d, qsd, s_sd, o["y"],
                           o["ysh"], mode=mode)
     m.moe_combine(w, T, o["y"], o["inv"], tw, o["ysh"], o["out"])
+    assert m.moe_check_status() == 0, m.last_error()
+    _assert_written(o)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("w", [TINY, MID8, WIDE], ids=lambda w: w.name)
+def test_forward_fp8_writes_every_output_element(w, mode):
+    T, k, H = w.tokens, w.top_k, w.hidden
+    x, wr, b, wg, wu, wd, sg, su, sd = _layer(w)
+    (qg, s_g), (qu, s_u), (qd, s_d) = _quant(wg), _quant(wu), _quant(wd)
+    (qsg, s_sg), (qsu, s_su) = _quant(sg), _quant(su)
+    qsd, s_sd = _quant(sd.permute(1, 0, 2).reshape(H, -1).contiguous())
+    o = dict(out=_f((T, H), torch.bfloat16), idx=_i((T, k)), tw=_f((T, k)), counts=_i((w.n_slots + 1,)),
+             blocks=_i((w.n_blocks,)))
+    ws = torch.empty(m.moe_workspace_size_fp8(w, T), dtype=torch.uint8, device=DEV)
+    m.moe_forward_fp8(w, T, x, wr, b, None, qg, s_g, qu, s_u, qd, s_d, qsg, s_sg, qsu, s_su, qsd, s_sd, o["out"],
+                      o["idx"], o["tw"], o["counts"], o["blocks"], mode=mode, ws=ws)
+    assert m.moe_check_status() == 0, m.last_error()
+    _assert_written(o)
+
+
+@pytest.mark.parametrize("w", [TINY, MID, WIDE], ids=lambda w: w.name)
+def test_grouped_route_histogram_and_ffn_write_every_output_element(w):
+    T, k, S, H, E = w.tokens, w.top_k, w.n_slots, w.hidden, w.n_experts
+    n = T * k
+    x, wr, b, wg, wu, wd, sg, su, sd = _layer(w)
+    groups = (w.n_blocks, max(1, w.n_blocks // 2))
+    o = dict(logits=_f((T, E)), idx=_i((T, k)), tw=_f((T, k)), counts=_i((S + 1,)), blocks=_i((w.n_blocks,)))
+    rws = torch.empty(max(16, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=DEV)
+    m.moe_route_grouped(w, T, groups[0], groups[1], x, wr, b, None, o["logits"], o["idx"], o["tw"], rws)
+    m.moe_expert_histogram(w, T, o["idx"], None, o["counts"], o["blocks"])
+    i32 = dict(dtype=torch.int32, device=DEV)
+    so, c, off = torch.empty(n, **i32), torch.empty(S + 1, **i32), torch.empty(S + 2, **i32)
+    perm, inv = torch.empty(n, **i32), torch.empty(n, **i32)
+    xd = torch.empty((n, H), dtype=torch.bfloat16, device=DEV)
+    m.moe_dispatch(w, T, x, o["idx"], None, so, c, None, off, perm, inv, xd)
+    o.update(y=_f((n, H), torch.bfloat16), ysh=_f((T, H)))
+    fws = torch.empty(max(16, m.moe_ffn_workspace_size(w, T)), dtype=torch.uint8, device=DEV)
+    m.moe_expert_ffn(w, T, x, xd, off, wg, wu, wd, sg, su, sd, o["y"], o["ysh"], m.MOE_FFN_AUTO, fws)
     assert m.moe_check_status() == 0, m.last_error()
     _assert_written(o)
