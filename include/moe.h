@@ -38,9 +38,9 @@
  *     error).  moe_expert_ffn_noalloc calls must not overlap (one scratch).
  *   - Calls enqueue kernels only and may be captured in a CUDA graph.  The
  *     first use of each kernel on a device sets its shared-memory attribute
- *     (cudaFuncSetAttribute), which a capture cannot record: make the same
- *     call (same entry point, shape and T) once before capturing it, as a
- *     warm-up does.
+ *     (cudaFuncSetAttribute, a host-side setting, not a graph node): make
+ *     the same call (same entry point, shape and T) once before capturing
+ *     it, as a warm-up does.
  *   - Calls of at most 8192 token-expert assignments (T*k) launch their
  *     kernels with programmatic dependent launch: a kernel may be scheduled
  *     while its predecessor in the stream finishes and waits for it before
