@@ -72,7 +72,7 @@ extern "C" {
 /* Status codes. */
 #define MOE_OK 0
 #define MOE_ERR_INVALID_ARG 1     /* null/misaligned pointer, bad size, inconsistent shape */
-#define MOE_ERR_UNSUPPORTED 2     /* valid shape outside this build's kernel limits */
+#define MOE_ERR_UNSUPPORTED 2     /* valid shape outside the library's kernel limits */
 #define MOE_ERR_CUDA 3            /* a CUDA runtime call or launch failed */
 #define MOE_ERR_DEVICE_TIMEOUT 4  /* a kernel's bounded wait expired (moe_check_status) */
 #define MOE_ERR_DEVICE_STATUS 5   /* a kernel flagged invalid data, e.g. expert id out of range */
@@ -88,7 +88,7 @@ extern "C" {
 #define MOE_FFN_DECODE 1
 #define MOE_FFN_PREFILL 2
 
-/* Layer shape.  Limits of this build: 1 <= k <= min(E, 32); E <= 1024;
+/* Layer shape.  Limits of the library: 1 <= k <= min(E, 32); E <= 1024;
  * S <= 1024; E and S divisible by B with S/B >= E/B; H, I, I_sh multiples of 8. */
 typedef struct {
     int32_t hidden;        /* H */

@@ -1,6 +1,6 @@
 """Degenerate and limit cases of the layer on the GPU against the fp64 oracle:
 one token, every expert selected, a single expert, no shared expert, the
-largest expert/slot counts and top-k this build accepts, an empty batch, and
+largest expert/slot counts and top-k the library accepts, an empty batch, and
 out-of-range expert ids reaching dispatch."""
 import numpy as np
 import pytest
