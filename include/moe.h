@@ -31,6 +31,8 @@
  *     wait that expired) set a device status word instead of faulting;
  *     moe_check_status() synchronises the stream, reads and clears it.
  *   - T = 0 is valid and enqueues nothing.
+ *   - Every *_workspace_size(shape, T) is non-decreasing in T: a workspace
+ *     sized for the largest batch serves every smaller one.
  *   - Any number of host threads may call concurrently, each on its own
  *     stream and buffers: the library's per-device set-up is done once under
  *     atomics, the error text is per thread, and the device status word is

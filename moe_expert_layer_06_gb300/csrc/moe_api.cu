@@ -226,10 +226,22 @@ static RoutePlan route_plan(const moe_shape_t* s, int T) {
     return p;
 }
 
+static size_t route_partials_bytes(const moe_shape_t* s, int T) {
+    const RoutePlan p = route_plan(s, T);
+    return (size_t)p.ksplit * T * s->n_experts * sizeof(float);
+}
+
+// The K-split partials of the largest need among batches of 1..T tokens, so a
+// workspace sized for the largest batch serves every smaller one.  The need
+// grows with T between token-chunk boundaries and drops after one (more tiles,
+// fewer K splits), so the maximum is at T or at a boundary below it; boundaries
+// stop mattering once the tiles fill the SMs (one K split).
 static size_t route_ws(const moe_shape_t* s, int T) {
     if (T == 0) return 0;
-    const RoutePlan p = route_plan(s, T);
-    return align256((size_t)p.ksplit * T * s->n_experts * sizeof(float));
+    size_t need = route_partials_bytes(s, T);
+    for (int j = 1; j <= num_sms() && (long)j * kPrefillBN < T; ++j)
+        need = std::max(need, route_partials_bytes(s, j * kPrefillBN));
+    return align256(need);
 }
 
 static int route_impl(const moe_shape_t* s, int T, int n_groups, int topk_groups, const void* x,

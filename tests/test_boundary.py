@@ -216,3 +216,14 @@ def test_eplb_window_and_migration_argument_checks():
     dup[7] = 65
     with pytest.raises(m.MoeError):
         m.moe_eplb_copy_replicas(w, old, dup, FAKE, FAKE, FAKE)
+
+
+def test_workspace_sizes_never_shrink_as_the_batch_grows():
+    """A workspace sized for the largest batch serves every smaller one."""
+    for name in ("tiny", "decode_t32", "redundant_t1024", "decode_t32_e1024"):
+        w = mi.WORKLOADS[name]
+        for fn in (m.moe_workspace_size, m.moe_workspace_size_fp8, m.moe_route_workspace_size,
+                   m.moe_ffn_workspace_size, m.moe_dispatch_workspace_size):
+            sizes = [fn(w, T) for T in range(0, 5000)]
+            drops = [T for T in range(1, len(sizes)) if sizes[T] < sizes[T - 1]]
+            assert not drops, (name, fn.__name__, drops[:3])
