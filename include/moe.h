@@ -136,6 +136,9 @@ MOE_API int moe_debug_expire_wait(void* stream);
  * NULL.  logits_in [T,E] fp32 or NULL: when given, the GEMM is skipped and the
  * selection runs on these final logits (bias must then be NULL; x, w_router
  * may be NULL).  logits_out [T,E] fp32 or NULL receives the logits used.
+ * The GEMM sums K in splits whose number follows T and the device's SM
+ * count, added in a fixed order: results repeat bit for bit on one GPU model
+ * and may differ in the last bits of the logits on another.
  * Outputs topk_idx [T,k] int32, topk_w [T,k] fp32.  ws: device workspace of
  * at least moe_route_workspace_size() bytes (may be NULL if that is 0). */
 MOE_API size_t moe_route_workspace_size(const moe_shape_t* shape, int T);
