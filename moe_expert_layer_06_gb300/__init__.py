@@ -140,6 +140,8 @@ def _ptr(t) -> Optional[int]:
     if isinstance(t, torch.Tensor):
         if t.numel() and not t.is_contiguous():
             raise ValueError("tensor must be contiguous")
+        if t.numel() and not t.is_cuda:  # the C ABI takes device pointers
+            raise ValueError("tensor must be on a CUDA device")
         return t.data_ptr() if t.numel() else None
     raise TypeError(type(t))
 

@@ -6,6 +6,7 @@ import os
 import re
 
 import numpy as np
+import torch
 import pytest
 
 import moe_expert_layer_06_gb300 as m
@@ -227,3 +228,13 @@ def test_workspace_sizes_never_shrink_as_the_batch_grows():
             sizes = [fn(w, T) for T in range(0, 5000)]
             drops = [T for T in range(1, len(sizes)) if sizes[T] < sizes[T - 1]]
             assert not drops, (name, fn.__name__, drops[:3])
+
+
+def test_binding_refuses_host_and_strided_tensors_before_calling_the_library():
+    w = mi.WORKLOADS["tiny"]
+    T, H = w.tokens, w.hidden
+    host = torch.zeros((T * w.top_k, H), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA device"):
+        m.moe_combine(w, T, host, None, None, None, torch.zeros((T, H), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="contiguous"):
+        m.moe_combine(w, T, host.t(), None, None, None, None)
