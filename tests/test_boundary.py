@@ -238,3 +238,26 @@ def test_binding_refuses_host_and_strided_tensors_before_calling_the_library():
         m.moe_combine(w, T, host, None, None, None, torch.zeros((T, H), dtype=torch.bfloat16))
     with pytest.raises(ValueError, match="contiguous"):
         m.moe_combine(w, T, host.t(), None, None, None, None)
+
+
+def test_fp8_argument_checks():
+    L = m.lib()
+    b = ctypes.c_void_p(FAKE)
+    # the row quantiser: rows >= 0, cols a positive multiple of 16; no rows is a no-op
+    assert L.moe_quantize_rows_fp8(-1, 64, b, b, b, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_rows_fp8(4, 24, b, b, b, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_rows_fp8(0, 64, None, None, None, None) == m.MOE_OK
+    # one-byte rows need H, I and n_sh*I_sh multiples of 16 (the bf16 path needs 8)
+    h8 = _shape(hidden=7176)
+    i8 = _shape(inter=2056)
+    sh8 = _shape(n_shared=1, inter_shared=2056)
+    assert L.moe_dispatch_fp8(ctypes.byref(h8), 32, *([b] * 13), None, 0, None) == m.MOE_ERR_INVALID_ARG
+    assert "16" in m.last_error()
+    assert L.moe_expert_gate_up_fp8(ctypes.byref(h8), 32, *([b] * 15), 0, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_expert_down_fp8(ctypes.byref(i8), 32, *([b] * 11), 0, None) == m.MOE_ERR_INVALID_ARG
+    assert L.moe_expert_down_fp8(ctypes.byref(sh8), 32, *([b] * 11), 0, None) == m.MOE_ERR_INVALID_ARG
+    for s in (h8, i8, sh8):
+        assert L.moe_forward_fp8(ctypes.byref(s), 32, *([b] * 21), 0, b, 1 << 40, None) == m.MOE_ERR_INVALID_ARG
+    ok = _shape()
+    assert L.moe_forward_fp8(ctypes.byref(ok), 32, *([b] * 21), 9, b, 1 << 40, None) == m.MOE_ERR_INVALID_ARG
+    assert "mode" in m.last_error()
