@@ -215,32 +215,36 @@ struct RoutePlan {
     int bn, ksplit, kc_split, tiles;
 };
 
-static RoutePlan route_plan(const moe_shape_t* s, int T) {
+static RoutePlan route_plan(const moe_shape_t* s, int T, int sms) {
     RoutePlan p;
     p.bn = T <= 32 ? 32 : kPrefillBN;
     const int kc = (s->hidden + 63) / 64;
     p.tiles = ((s->n_experts + 127) / 128) * ((T + p.bn - 1) / p.bn);
-    const int want = std::max(1, (num_sms() + p.tiles - 1) / std::max(1, p.tiles));
+    const int want = std::max(1, (sms + p.tiles - 1) / std::max(1, p.tiles));
     p.kc_split = std::max(1, (kc + want - 1) / want);
     p.ksplit = (kc + p.kc_split - 1) / p.kc_split;
     return p;
 }
 
-static size_t route_partials_bytes(const moe_shape_t* s, int T) {
-    const RoutePlan p = route_plan(s, T);
+static RoutePlan route_plan(const moe_shape_t* s, int T) { return route_plan(s, T, num_sms()); }
+
+static size_t route_partials_bytes(const moe_shape_t* s, int T, int sms) {
+    const RoutePlan p = route_plan(s, T, sms);
     return (size_t)p.ksplit * T * s->n_experts * sizeof(float);
 }
 
 // The K-split partials of the largest need among batches of 1..T tokens, so a
 // workspace sized for the largest batch serves every smaller one.  The need
 // grows with T between token-chunk boundaries and drops after one (more tiles,
-// fewer K splits), so the maximum is at T or at a boundary below it; boundaries
-// stop mattering once the tiles fill the SMs (one K split).
+// fewer K splits), so the maximum is at T or at a boundary below it; a boundary
+// whose tiles fill the SMs has one K split and cannot exceed the need at T.
 static size_t route_ws(const moe_shape_t* s, int T) {
     if (T == 0) return 0;
-    size_t need = route_partials_bytes(s, T);
-    for (int j = 1; j <= num_sms() && (long)j * kPrefillBN < T; ++j)
-        need = std::max(need, route_partials_bytes(s, j * kPrefillBN));
+    const int sms = num_sms();
+    const long row_tiles = (s->n_experts + 127) / 128;
+    size_t need = route_partials_bytes(s, T, sms);
+    for (long j = 1; j * kPrefillBN < T && j * row_tiles < sms; ++j)
+        need = std::max(need, route_partials_bytes(s, (int)(j * kPrefillBN), sms));
     return align256(need);
 }
 
