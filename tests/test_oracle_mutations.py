@@ -47,8 +47,8 @@ MUTANTS = [
      "const float s = amax > 0.0f ? amax / 240.0f : 1.0f;"),
     ("fp8 gate ignores the token scale", "g *= (double)sx * (double)sg[i];", "g *= (double)sg[i];"),
     ("fp8 down ignores the weight-row scale", "y[o] = acc * (double)sh * (double)sd[o];", "y[o] = acc * (double)sh;"),
-    ("fp8 down reads its weights transposed", "oracle_e4m3_decode(qd[(size_t)o * K + i]);",
-     "oracle_e4m3_decode(qd[(size_t)i * H + o]);"),
+    ("fp8 down reads its weights transposed", "dec[qd[(size_t)o * K + i]];",
+     "dec[qd[(size_t)i * H + o]];"),
     ("bf16 rounding truncates", "const double r = rint(v / step) * step;", "const double r = trunc(v / step) * step;"),
     ("home slot ignores the replica slots", "return (e / epb) * spb + (e % epb);", "return e;"),
     ("replica used by even tokens", "replica_of[e] >= 0 && (t % 2) == 1", "replica_of[e] >= 0 && (t % 2) == 0"),
