@@ -33,11 +33,39 @@ def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, (e - 8).astype(np.int64))
 
 
-def assert_close(got, want, rel_frob=REL_FROB, elem_rms=ELEM_RMS, what="", bf16_out=True):
+# Elements with |ref| <= PLAIN_BOUND_RMS * rms(ref) are held to the scope's bound
+# elem_rms * rms(ref) alone, without the half-ulp allowance: there the output's
+# own bf16 rounding is at most PLAIN_BOUND_RMS * rms * 2^-8 (0.0156 rms), about
+# half of the bound, which leaves the other half for the arithmetic.
+PLAIN_BOUND_RMS = 4.0
+
+
+def _report(record: dict) -> None:
+    """Append one JSON line to $MOE_PARITY_REPORT (if set): the numbers the
+    parity tests measured (errors, near-tie counts, sample sizes)."""
+    path = os.environ.get("MOE_PARITY_REPORT")
+    if not path:
+        return
+    import json
+    with open(path, "a") as f:
+        f.write(json.dumps(record) + "\n")
+
+
+def assert_close(got, want, rel_frob=REL_FROB, elem_rms=ELEM_RMS, what="", bf16_out=True, e4m3_layer=False):
     """Relative Frobenius error <= rel_frob and every |err| <= elem_rms * rms(want),
     plus, for a bf16 output compared with the unrounded oracle, half the bf16
     spacing at that element (a value between two bf16 numbers is at least
-    that far from both)."""
+    that far from both); elements with |want| <= PLAIN_BOUND_RMS * rms(want)
+    must meet elem_rms * rms(want) without that allowance, except in an E4M3
+    layer's output (e4m3_layer): there the kernel quantises its own fp32
+    intermediate and the oracle its fp64 one, so an intermediate code can
+    differ by one step where the two round to different bf16 values, an
+    error of its own beside the output's rounding; those outputs report the
+    count without asserting it.
+
+    Returns a dict: rel_frob, worst |err|/rms, how many elements exceed the
+    plain bound (and so rely on the half-ulp allowance), and the largest
+    |want|/rms among them."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (got.shape, want.shape)
@@ -47,14 +75,28 @@ def assert_close(got, want, rel_frob=REL_FROB, elem_rms=ELEM_RMS, what="", bf16_
     rel = np.linalg.norm(err) / nw if nw > 0 else np.linalg.norm(err)
     rms = np.sqrt(np.mean(want ** 2)) if want.size else 0.0
     assert rel <= rel_frob, f"{what}: relative Frobenius error {rel:.3e} > {rel_frob}"
+    stats = dict(what=what, elements=int(err.size), rel_frob=float(rel), worst_err_over_rms=0.0,
+                 over_plain_bound=0, max_ref_over_rms_over_plain_bound=0.0)
     if err.size:
-        bound = elem_rms * rms + 1e-30 + (bf16_half_ulp(want) if bf16_out else 0.0)
+        plain = elem_rms * rms + 1e-30
+        bound = plain + (bf16_half_ulp(want) if bf16_out else 0.0)
         worst = np.argmax(np.abs(err) - bound)
         e_w, b_w = np.abs(err).ravel()[worst], np.broadcast_to(bound, err.shape).ravel()[worst]
         assert e_w <= b_w, (f"{what}: |err| {e_w:.3e} > bound {b_w:.3e} ({elem_rms}*rms {elem_rms * rms:.3e}"
                             f"{' + half bf16 ulp' if bf16_out else ''}) at value {want.ravel()[worst]:.4g}")
-    mx = np.abs(err).max() if err.size else 0.0
-    return rel, mx / rms if rms else 0.0
+        over = np.abs(err) > plain
+        inner = np.abs(want) <= PLAIN_BOUND_RMS * rms
+        bad = np.flatnonzero((over & inner).ravel())
+        assert e4m3_layer or bad.size == 0, (f"{what}: {bad.size} elements with |ref| <= {PLAIN_BOUND_RMS}*rms exceed "
+                               f"{elem_rms}*rms without the half-ulp allowance, e.g. |err| "
+                               f"{np.abs(err).ravel()[bad[0]]:.3e} at value {want.ravel()[bad[0]]:.4g}")
+        stats["worst_err_over_rms"] = float(np.abs(err).max() / rms) if rms else 0.0
+        stats["over_plain_bound"] = int(over.sum())
+        if over.any():
+            stats["max_ref_over_rms_over_plain_bound"] = float(np.abs(want[over]).max() / rms)
+            stats["inner_over_plain_bound"] = int(bad.size)
+    _report(dict(stats, kind="assert_close"))
+    return stats
 
 
 def topk_gap(logits: np.ndarray, k: int) -> np.ndarray:
@@ -176,30 +218,118 @@ class DeviceLayer:
         return dict(out=out, idx=idx, w=tw, counts=counts, blocks=blocks)
 
 
-def oracle_token_rows(w, tokens, x_cpu, wr_cpu, bias, replica_of=None, expert_cache=None, groups=None):
-    """Oracle routing and output for a sample of tokens of a full-size workload
-    (groups = (n_groups, topk_groups) for group-limited routing).
+# ----------------------------------------------------------------------------- full-size sampled parity
 
-    Only the experts those tokens select are generated (on the CPU).
+SAMPLE_TOKENS = 256   # tokens per full-size workload checked element by element (all of them if fewer)
+SAMPLE_SEED = 20261203
+
+
+def sample_tokens(sure, n=SAMPLE_TOKENS, seed=SAMPLE_SEED) -> np.ndarray:
+    """A seeded uniform sample of n tokens among those whose top-k selection is
+    decided (all of them when there are at most n), ascending."""
+    cand = np.flatnonzero(np.asarray(sure))
+    if cand.size <= n:
+        return cand
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return np.sort(rng.choice(cand, size=n, replace=False))
+
+
+def check_counts_of_routing(w, idx_gpu, counts_gpu, blocks_gpu, rep=None, idx_oracle=None, sure=None):
+    """The GPU's per-slot counts and block loads equal the oracle's remap and
+    histogram of the GPU's own top-k selection (always), and of the oracle's
+    selection when every token's selection is decided.  Returns the number of
+    near-tie tokens (top-k gap <= TOPK_GAP)."""
+    so, invalid = oracle.slot_map(w, np.asarray(idx_gpu), rep)
+    assert invalid == 0
+    c_o, b_o = oracle.histogram(w, so)
+    assert np.array_equal(np.asarray(counts_gpu), c_o), "per-slot counts differ from the oracle's histogram"
+    assert np.array_equal(np.asarray(blocks_gpu), b_o), "block loads differ from the oracle's histogram"
+    ties = 0 if sure is None else int((~np.asarray(sure)).sum())
+    if idx_oracle is not None and ties == 0:
+        so2, _ = oracle.slot_map(w, idx_oracle, rep)
+        c2, b2 = oracle.histogram(w, so2)
+        assert np.array_equal(np.asarray(counts_gpu), c2) and np.array_equal(np.asarray(blocks_gpu), b2)
+    return ties
+
+
+def _pool_map(fn, items):
+    with cf.ThreadPoolExecutor(min(THREADS, max(1, len(items)))) as ex:
+        return list(ex.map(fn, items))
+
+
+def oracle_sampled_layer(w, toks, x_cpu, idx, weight, expert_host, shared, fp8=False, window=16):
+    """The oracle's layer output [len(toks), H] for the sampled tokens, given
+    their selection idx[t] and combine weights weight[t] (oracle routing).
+
+    Expert-major: the experts the sample selects are fetched `window` at a
+    time through expert_host(e) -> (gate [I,H], up [I,H], down [H,I]) bf16 on
+    the host, every (token, expert) pair of the window is computed by the
+    oracle on the host threads, then the shared experts and the combine, in
+    the oracle's order (j ascending, shared last).  fp8: the same with the
+    layer's E4M3 quantisation, the oracle quantising each fetched expert's
+    rows; shared = the oracle's E4M3 shared matrices (quantize_layer_fp8 keys
+    qsg, ssg, qsu, ssu, qsd, ssd), else (gate, up, down) stacked bf16.
     """
-    expert_cache = {} if expert_cache is None else expert_cache
-    xs = x_cpu[tokens]
-    logits = oracle.router_logits(w, xs, wr_cpu, bias)
-    if groups is None:
-        idx, wt = oracle.topk_softmax(logits, w.top_k)
+    toks = np.asarray(toks)
+    n, k, H = len(toks), w.top_k, w.hidden
+    xs = x_cpu[torch.as_tensor(toks, dtype=torch.long)]
+    if fp8:
+        qx, sx = oracle.quantize_rows_e4m3(xs)
+    pairs = {}
+    for i, t in enumerate(toks):
+        for j in range(k):
+            pairs.setdefault(int(idx[t, j]), []).append((i, j))
+    y = np.zeros((n * k, H), dtype=np.float64)
+    experts = sorted(pairs)
+    for e0 in range(0, len(experts), window):
+        group = experts[e0:e0 + window]
+        mats = dict(zip(group, _pool_map(lambda e: tuple(a.contiguous() for a in expert_host(e)), group)))
+        if fp8:
+            flat = [(e, a) for e in group for a in range(3)]
+            q = _pool_map(lambda ea: oracle.quantize_rows_e4m3(mats[ea[0]][ea[1]]), flat)
+            mats = {e: tuple(q[3 * gi + a] for a in range(3)) for gi, e in enumerate(group)}
+
+        def one(job):
+            e, i, j = job
+            if fp8:
+                (cg, scg), (cu, scu), (cd, scd) = mats[e]
+                y[i * k + j] = oracle.swiglu_row_fp8(qx[i], sx[i], cg, scg, cu, scu, cd, scd)
+            else:
+                y[i * k + j] = oracle.swiglu_row(xs[i], *mats[e])
+
+        _pool_map(one, [(e, i, j) for e in group for (i, j) in pairs[e]])
+        del mats
+    if w.n_shared == 0:
+        ysh = np.zeros((n, H))
+    elif fp8:
+        ysh = np.stack(_pool_map(lambda i: oracle.shared_row_fp8(w, qx[i], sx[i], shared), range(n)))
     else:
-        idx, wt = oracle.topk_grouped(logits, w.top_k, *groups)
-    need = sorted(set(int(e) for e in idx.ravel()) - set(expert_cache))
-    for e in need:
-        expert_cache[e] = mi.expert_weights(w, e)
-    sg, su, sd = mi.stacked_shared_weights(w)
+        sg, su, sd = shared
+        ysh = np.concatenate(_pool_map(lambda i: oracle.shared_rows(w, xs[i:i + 1], sg, su, sd), range(n)))
+    wt = np.ascontiguousarray(np.asarray(weight)[toks], dtype=np.float64)
+    return oracle.combine(w.with_(tokens=n), n, y, np.arange(n * k, dtype=np.int32), wt, ysh)
 
-    def one(i):
-        gud = [expert_cache[int(e)] for e in idx[i]]
-        ys = [oracle.swiglu_row(xs[i], *g) for g in gud]
-        out = oracle.token_output(w, xs[i], wt[i], gud, sg, su, sd)
-        return ys, out
 
-    with cf.ThreadPoolExecutor(min(THREADS, len(tokens))) as ex:
-        res = list(ex.map(one, range(len(tokens))))
-    return dict(logits=logits, idx=idx, weight=wt, y=[r[0] for r in res], out=np.stack([r[1] for r in res]))
+def check_full_size_layer(w, out_gpu, idx_gpu, counts_gpu, blocks_gpu, expert_host, shared, rep=None, fp8=False,
+                          n_sample=SAMPLE_TOKENS, what=""):
+    """Parity of a full-size layer pass against the oracle.
+
+    Routing of every token (oracle logits in fp64 on the host threads): top-k
+    sets and order where decided; counts and block loads of the GPU's own
+    routing, unconditionally.  Output: n_sample seeded random tokens with a
+    decided selection, element by element.  Returns the report record."""
+    x = mi.hidden_states(w)
+    wr = mi.router_weight(w)
+    b = mi.router_bias(w)
+    lo = parallel_router_logits(w, x, wr, b)
+    idx_o, wt_o = oracle.topk_softmax(lo, w.top_k)
+    idx_g = np.asarray(idx_gpu)
+    sure = check_topk(idx_g, idx_o, lo, w.top_k)
+    ties = check_counts_of_routing(w, idx_g, counts_gpu, blocks_gpu, rep, idx_o, sure)
+    toks = sample_tokens(sure, n_sample)
+    ref = oracle_sampled_layer(w, toks, x, idx_o, wt_o, expert_host, shared, fp8=fp8)
+    stats = assert_close(np.asarray(out_gpu)[toks], ref, what=what or f"{w.name} sampled out", e4m3_layer=fp8)
+    rec = dict(stats, kind="full_size_layer", workload=w.name, precision="e4m3" if fp8 else "bf16",
+               tokens=int(w.tokens), sampled_tokens=int(len(toks)), near_tie_tokens=ties)
+    _report(rec)
+    return rec

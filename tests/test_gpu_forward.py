@@ -2,9 +2,10 @@
 
 Small shapes: the oracle computes the whole layer.  The DeepSeek-V3 shapes
 (decode T=32, skewed decode T=256, prefill T=4096, redundant experts T=1024):
-the oracle computes the routing of every token and the full output of a
-sample of tokens (only their experts are generated on the host), and the
-launch configuration is the one bench.py times.
+the oracle computes the routing of every token and the full output of 256
+seeded random tokens (every token at T=32), and the launch configuration is
+the one bench.py times.  Per-slot counts and block loads are checked on every
+call against the oracle's histogram of the GPU's own selection.
 """
 import numpy as np
 import pytest
@@ -13,8 +14,8 @@ import torch
 import moe_expert_layer_06_gb300 as m
 import moe_inputs as mi
 import oracle
-from moe_testlib import (grouped_sure, DeviceLayer, assert_close, check_topk, oracle_token_rows, parallel_router_logits,
-                         to_np)
+from moe_testlib import (SAMPLE_TOKENS, DeviceLayer, assert_close, check_counts_of_routing, check_full_size_layer,
+                         check_topk, grouped_sure, oracle_sampled_layer, parallel_router_logits, sample_tokens, to_np)
 from test_gpu_stages import DEEP, MID, REP
 
 pytestmark = pytest.mark.gpu
@@ -46,10 +47,9 @@ def test_forward_small_matches_oracle(name, mode):
     ref = oracle.moe_forward(w, x, wr, b, rep, wg, wu, wd, sg, su, sd)
     layer = DeviceLayer(w, DEV, replica_of=rep)
     r = layer.forward(mode)
-    sure = check_topk(r["idx"].cpu().numpy(), ref["idx"], ref["logits"], w.top_k)
-    if sure.all():
-        assert np.array_equal(r["counts"].cpu().numpy(), ref["counts"])
-        assert np.array_equal(r["blocks"].cpu().numpy(), ref["block_counts"])
+    idx_g = r["idx"].cpu().numpy()
+    sure = check_topk(idx_g, ref["idx"], ref["logits"], w.top_k)
+    check_counts_of_routing(w, idx_g, r["counts"].cpu().numpy(), r["blocks"].cpu().numpy(), rep, ref["idx"], sure)
     assert_close(to_np(r["out"])[sure], ref["out"][sure], what=f"{name} out")
 
 
@@ -64,8 +64,6 @@ def test_generator_is_identical_on_cpu_and_gpu():
 
 # ----------------------------------------------------------------------------- full size
 
-_EXPERTS_CPU = {}
-
 
 @pytest.fixture(scope="module")
 def dsv3_weights():
@@ -73,36 +71,44 @@ def dsv3_weights():
     return mi.stacked_expert_weights(w, device=DEV)
 
 
-def _sample_tokens(T, sure, n=3):
-    cand = [0, T // 3, (2 * T) // 3 + 1, T - 1]
-    out = [t for t in cand if sure[t]]
-    return out[:n] if out else [int(np.flatnonzero(sure)[0])]
+def test_generator_rows_of_every_expert_match_on_cpu_and_gpu(dsv3_weights):
+    """The full-size parity tests give the oracle the generator's expert
+    weights as generated on the device (regenerating 22.5 GB on the host would
+    take minutes): two seeded rows of every expert matrix regenerated on the
+    host match the device copies bit for bit."""
+    w = mi.WORKLOADS["decode_t32"]
+    H, I = w.hidden, w.inter
+    rng = np.random.Generator(np.random.PCG64(5))
+    wg, wu, wd = dsv3_weights
+    for e in range(w.n_experts):
+        for t, tid, rows, cols, fan in ((wg, mi.TID_GATE, I, H, H), (wu, mi.TID_UP, I, H, H),
+                                        (wd, mi.TID_DOWN, H, I, I)):
+            for r in rng.integers(0, rows, 2):
+                host = mi.normal_bf16((cols,), 1.0 / np.sqrt(fan), w.seed, tid, e, offset=int(r) * cols)
+                assert torch.equal(t[e, int(r)].cpu(), host), (e, tid, int(r))
 
 
-def _check_full(w, layer, rep=None, n_sample=3):
-    r = layer.forward()
-    x = mi.hidden_states(w)
-    wr = mi.router_weight(w)
-    b = mi.router_bias(w)
-    lo = parallel_router_logits(w, x, wr, b)
-    idx_o, _ = oracle.topk_softmax(lo, w.top_k)
-    sure = check_topk(r["idx"].cpu().numpy(), idx_o, lo, w.top_k)
-    if sure.all():
-        so, _ = oracle.slot_map(w, idx_o, rep)
-        c_o, b_o = oracle.histogram(w, so)
-        assert np.array_equal(r["counts"].cpu().numpy(), c_o)
-        assert np.array_equal(r["blocks"].cpu().numpy(), b_o)
-    toks = _sample_tokens(w.tokens, sure, n_sample)
-    ref = oracle_token_rows(w, toks, x, wr, b, rep, _EXPERTS_CPU)
-    assert_close(to_np(r["out"])[toks], ref["out"], what=f"{w.name} sampled out")
-    return r
+def _host_experts(weights):
+    """expert_host(e) for the oracle: logical expert e's matrices copied from the
+    device stack of the 256 experts (slot e holds expert e there)."""
+    return lambda e: tuple(t[e].cpu() for t in weights)
+
+
+def _check_full(w, r, weights, rep=None, n_sample=SAMPLE_TOKENS):
+    sh = mi.stacked_shared_weights(w)
+    return check_full_size_layer(w, to_np(r["out"]), r["idx"].cpu().numpy(), r["counts"].cpu().numpy(),
+                                 r["blocks"].cpu().numpy(), _host_experts(weights), sh, rep=rep,
+                                 n_sample=n_sample)
 
 
 @pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew", "prefill_t4096"])
 def test_forward_full_size(name, dsv3_weights):
+    """The layer at the bench's launch configuration: every token's routing,
+    the counts of the GPU's own routing, and 256 seeded random tokens' outputs
+    (all 32 at T=32) element by element against the oracle."""
     w = mi.WORKLOADS[name]
     layer = DeviceLayer(w, DEV, weights=dsv3_weights)
-    _check_full(w, layer)
+    _check_full(w, layer.forward(), dsv3_weights)
 
 
 def test_redundant_experts_full_size(dsv3_weights):
@@ -119,7 +125,8 @@ def test_redundant_experts_full_size(dsv3_weights):
     assert int((se < 0).sum()) == 0
     weights = tuple(t.index_select(0, se) for t in dsv3_weights)
     layer = DeviceLayer(w, DEV, replica_of=rep, weights=weights)
-    r = _check_full(w, layer, rep)
+    r = layer.forward()
+    _check_full(w, r, dsv3_weights, rep)
     c = r["counts"].cpu().numpy()
     assert c.sum() == w.tokens * w.top_k and c[-1] == 0
     # the replicated layer gives the non-replicated layer's output
@@ -135,21 +142,25 @@ def test_redundant_experts_full_size(dsv3_weights):
 @pytest.mark.parametrize("groups", [None, (8, 4)])
 def test_forward_full_size_1024_experts(groups):
     """1024 experts of the DeepSeek-V3 shape (90 GB of bf16 weights), plain and
-    group-limited routing (8 groups, 4 kept): sampled tokens against the oracle."""
+    group-limited routing (8 groups, 4 kept): every token of the batch against
+    the oracle."""
     w = mi.WORKLOADS["decode_t32_e1024"]
     weights = mi.stacked_expert_weights(w, device=DEV)
     layer = DeviceLayer(w, DEV, weights=weights)
     if groups is None:
-        _check_full(w, layer, n_sample=2)
+        _check_full(w, layer.forward(), weights)
     else:
-        T, k = w.tokens, w.top_k
+        k = w.top_k
         r = layer.forward_grouped(*groups)
         x, wr = mi.hidden_states(w), mi.router_weight(w)
         lo = parallel_router_logits(w, x, wr, None)
         sure, idx_o = grouped_sure(lo, k, *groups)
-        assert np.array_equal(r["idx"].cpu().numpy()[sure], idx_o[sure])
-        toks = _sample_tokens(T, sure, 2)
-        ref = oracle_token_rows(w, toks, x, wr, None, None, _EXPERTS_CPU, groups=groups)
-        assert_close(to_np(r["out"])[toks], ref["out"], what="1024 experts, group-limited, sampled out")
+        idx_g = r["idx"].cpu().numpy()
+        assert np.array_equal(idx_g[sure], idx_o[sure])
+        check_counts_of_routing(w, idx_g, r["counts"].cpu().numpy(), r["blocks"].cpu().numpy())
+        _, wt_o = oracle.topk_grouped(lo, k, *groups)
+        toks = sample_tokens(sure)
+        ref = oracle_sampled_layer(w, toks, x, idx_o, wt_o, _host_experts(weights), mi.stacked_shared_weights(w))
+        assert_close(to_np(r["out"])[toks], ref, what="1024 experts, group-limited")
     del weights, layer
     torch.cuda.empty_cache()

@@ -13,7 +13,7 @@ import torch
 import moe_expert_layer_06_gb300 as m
 import moe_inputs as mi
 import oracle
-from moe_testlib import assert_close, check_topk, parallel_router_logits, to_np
+from moe_testlib import assert_close, check_full_size_layer, check_topk, parallel_router_logits, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -231,14 +231,18 @@ def test_fp8_layer_matches_fp8_oracle(name, mode):
                       ws=ws)
     assert m.moe_check_status() == 0, m.last_error()
     sure = check_topk(idx.cpu().numpy(), ref["idx"], lo, w.top_k)
-    assert_close(to_np(out)[sure], ref["out"][sure], what=f"{name} fp8 layer")
-
-
-_EXPERTS = {}
+    assert_close(to_np(out)[sure], ref["out"][sure], what=f"{name} fp8 layer", e4m3_layer=True)
 
 
 @pytest.fixture(scope="module")
-def fp8_dsv3():
+def dsv3_bf16():
+    """The 256 DeepSeek-V3-shaped experts in bf16 on the device: the source of
+    the device E4M3 copies and of the host copies the oracle quantises itself."""
+    return mi.stacked_expert_weights(mi.WORKLOADS["decode_t32"], device=DEV)
+
+
+@pytest.fixture(scope="module")
+def fp8_dsv3(dsv3_bf16):
     """Every DeepSeek-V3-shaped expert and shared matrix quantised on the device
     (the quantiser itself is pinned bit-exact above)."""
     w = mi.WORKLOADS["decode_t32"]
@@ -248,12 +252,11 @@ def fp8_dsv3():
         q = torch.empty(t.shape, dtype=torch.uint8, device=DEV)
         sc = torch.empty(t.numel() // t.shape[-1], dtype=torch.float32, device=DEV)
         m.moe_quantize_rows_fp8(t.view(-1, t.shape[-1]), q, sc)
-        return q, sc
+        return q, sc.view(t.shape[:-1])
 
     d = {}
-    wg, wu, wd = mi.stacked_expert_weights(w, device=DEV)
+    wg, wu, wd = dsv3_bf16
     (d["qg"], d["sg"]), (d["qu"], d["su"]), (d["qd"], d["sd"]) = quant(wg), quant(wu), quant(wd)
-    del wg, wu, wd
     sg, su, sd = mi.stacked_shared_weights(w, device=DEV)
     (d["qsg"], d["ssg"]), (d["qsu"], d["ssu"]) = quant(sg), quant(su)
     d["qsd"], d["ssd"] = quant(sd.permute(1, 0, 2).reshape(H, -1).contiguous())
@@ -262,47 +265,51 @@ def fp8_dsv3():
     return d
 
 
-# T = 32 runs the 32-row chunk, the skewed T = 256 batch the 160-row gate/up and
-# the 128-row down chunk of the automatic mode (hot experts hold more than one)
-@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew"])
-def test_fp8_layer_full_shape_sampled_tokens(name, fp8_dsv3):
+def _replica_plan_of_skewed_batch(w):
+    src = mi.WORKLOADS[mi.REPLICA_PLAN_SOURCE]
+    lo = parallel_router_logits(src, mi.hidden_states(src), mi.router_weight(src), mi.router_bias(src))
+    idx_src, _ = oracle.topk_softmax(lo, src.top_k)
+    return oracle.plan_replicas(w, np.bincount(idx_src.ravel(), minlength=w.n_experts), mi.N_REPLICAS)
+
+
+# decode T=32 runs the 32-row chunk, the skewed T=256 batch the 160-row gate/up
+# and the 128-row down chunk of the automatic mode (hot experts hold more than
+# one), prefill T=4096 the 160-row chunks with the chunked index pass, the
+# redundant T=1024 batch the replica slots
+@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew", "prefill_t4096", "redundant_t1024"])
+def test_fp8_layer_full_shape(name, dsv3_bf16, fp8_dsv3):
+    """The E4M3 layer at the bench's launch configuration against the oracle's
+    E4M3 layer: every token's routing, the counts of the GPU's own routing, and
+    256 seeded random tokens' outputs (all 32 at T=32) element by element."""
     w = mi.WORKLOADS[name]
-    T, H, k = w.tokens, w.hidden, w.top_k
-    d = fp8_dsv3
+    T, H, k, S = w.tokens, w.hidden, w.top_k, w.n_slots
+    d = dict(fp8_dsv3)
+    rep = None
+    if S > w.n_experts:
+        rep = _replica_plan_of_skewed_batch(w)
+        se = torch.from_numpy(mi.slot_experts(w, rep)).to(DEV)
+        for key in ("qg", "sg", "qu", "su", "qd", "sd"):
+            d[key] = d[key].index_select(0, se)
     x = mi.hidden_states(w)
-    wr = mi.router_weight(w)
     b = mi.router_bias(w)
+    i32 = dict(dtype=torch.int32, device=DEV)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
-    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
-    tw = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    idx, counts, blocks = torch.empty((T, k), **i32), torch.empty(S + 1, **i32), torch.empty(w.n_blocks, **i32)
     ws = torch.empty(m.moe_workspace_size_fp8(w, T), dtype=torch.uint8, device=DEV)
     bd = torch.from_numpy(b).to(DEV) if b is not None else None
-    m.moe_forward_fp8(w, T, x.to(DEV), wr.to(DEV), bd, None, d["qg"], d["sg"],
-                      d["qu"], d["su"], d["qd"], d["sd"], d["qsg"], d["ssg"], d["qsu"], d["ssu"], d["qsd"], d["ssd"],
-                      out, topk_idx_out=idx, topk_w_out=tw, ws=ws)
+    repd = torch.from_numpy(rep).to(DEV) if rep is not None else None
+    m.moe_forward_fp8(w, T, x.to(DEV), mi.router_weight(w, device=DEV), bd, repd, d["qg"], d["sg"], d["qu"],
+                      d["su"], d["qd"], d["sd"], d["qsg"], d["ssg"], d["qsu"], d["ssu"], d["qsd"], d["ssd"], out,
+                      topk_idx_out=idx, counts_out=counts, block_counts_out=blocks, ws=ws)
     assert m.moe_check_status() == 0, m.last_error()
-    lo = parallel_router_logits(w, x, wr, b)
-    idx_o, wt_o = oracle.topk_softmax(lo, k)
-    sure = check_topk(idx.cpu().numpy(), idx_o, lo, k)
     if name == "decode_t256_skew":
-        assert np.bincount(idx_o.ravel(), minlength=w.n_experts).max() > 128  # a two-chunk expert is present
-    toks = [t for t in (0, T // 3, (2 * T) // 3 + 1, T - 1) if sure[t]][:3]
-    assert toks
-    qx, sx = oracle.quantize_rows_e4m3(x)
+        assert int(counts.max()) > 128  # a two-chunk expert is present
+    del d
     sgc, suc, sdc = mi.stacked_shared_weights(w)
     qsh = {}
     qsh["qsg"], qsh["ssg"] = oracle.quantize_rows_e4m3(sgc.reshape(-1, H))
     qsh["qsu"], qsh["ssu"] = oracle.quantize_rows_e4m3(suc.reshape(-1, H))
     qsh["qsd"], qsh["ssd"] = oracle.quantize_rows_e4m3(oracle.shared_down_matrix(sdc))
-    for t in toks:
-        ys = []
-        for e in idx_o[t]:
-            if int(e) not in _EXPERTS:
-                g, u, dn = mi.expert_weights(w, int(e))
-                _EXPERTS[int(e)] = tuple(oracle.quantize_rows_e4m3(a) for a in (g, u, dn))
-            (cg, scg), (cu, scu), (cd, scd) = _EXPERTS[int(e)]
-            ys.append(oracle.swiglu_row_fp8(qx[t], sx[t], cg, scg, cu, scu, cd, scd))
-        ysh = oracle.shared_row_fp8(w, qx[t], sx[t], qsh)
-        ref = oracle.combine(w.with_(tokens=1), 1, np.stack(ys), np.arange(k, dtype=np.int32), wt_o[t:t + 1],
-                             ysh[None, :])
-        assert_close(to_np(out)[t:t + 1], ref, what=f"fp8 {name} token {t}")
+    check_full_size_layer(w, to_np(out), idx.cpu().numpy(), counts.cpu().numpy(), blocks.cpu().numpy(),
+                          lambda e: tuple(t[e].cpu() for t in dsv3_bf16), qsh, rep=rep, fp8=True,
+                          what=f"{name} E4M3 sampled out")
