@@ -288,6 +288,33 @@ def quantize_rows_e4m3(x):
     return codes.reshape(xs.shape), scale
 
 
+PAYLOAD_BLOCK = 128  # columns per scale of the E4M3 combine payload (ORACLE_PAYLOAD_BLOCK)
+
+
+def quantize_blocks_e4m3(x, block: int):
+    """Per-(row, block of `block` columns) E4M3 codes [R, C] and fp32 scales [R, ceil(C/block)]."""
+    xs = _u16(x)
+    R, C = xs.shape[0], int(np.prod(xs.shape[1:]))
+    nb = (C + block - 1) // block
+    codes = np.empty((R, C), dtype=np.uint8)
+    scale = np.empty((R, nb), dtype=np.float32)
+    lib().oracle_quantize_blocks_e4m3(R, C, block, _ptr(xs), _ptr(codes), _ptr(scale))
+    return codes, scale
+
+
+def payload_e4m3(y):
+    """The E4M3 combine payload of expert output rows y [R, H] (float64):
+    returns (dequantised y [R, H] float64, codes [R, H] uint8, scales [R, nb] float32)."""
+    yy = _f64(y)
+    R, C = yy.shape
+    nb = (C + PAYLOAD_BLOCK - 1) // PAYLOAD_BLOCK
+    deq = np.empty((R, C), dtype=np.float64)
+    codes = np.empty((R, C), dtype=np.uint8)
+    scale = np.empty((R, nb), dtype=np.float32)
+    lib().oracle_payload_e4m3(R, C, _ptr(yy), _ptr(deq), _ptr(codes), _ptr(scale))
+    return deq, codes, scale
+
+
 def bf16_round(values) -> np.ndarray:
     """Nearest bf16 (ties to even) of each value, as uint16 bit patterns."""
     f = lib().oracle_double_to_bf16

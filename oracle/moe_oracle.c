@@ -466,6 +466,35 @@ void oracle_quantize_rows_e4m3(int rows, int cols, const uint16_t* x_bf16, uint8
     }
 }
 
+void oracle_quantize_blocks_e4m3(int rows, int cols, int block, const uint16_t* x_bf16, uint8_t* codes,
+                                 float* scale) {
+    const int nb = (cols + block - 1) / block;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < nb; ++b) {
+            const int c0 = b * block;
+            const int w = cols - c0 < block ? cols - c0 : block;
+            oracle_quantize_rows_e4m3(1, w, x_bf16 + (size_t)r * cols + c0, codes + (size_t)r * cols + c0,
+                                      scale + (size_t)r * nb + b);
+        }
+}
+
+void oracle_payload_e4m3(int rows, int cols, const double* y, double* y_deq, uint8_t* codes, float* scale) {
+    const int nb = (cols + ORACLE_PAYLOAD_BLOCK - 1) / ORACLE_PAYLOAD_BLOCK;
+    uint16_t* yb = (uint16_t*)malloc((size_t)cols * sizeof(uint16_t));
+    uint8_t* q = (uint8_t*)malloc((size_t)cols);
+    float* sc = (float*)malloc((size_t)nb * sizeof(float));
+    for (int r = 0; r < rows; ++r) {
+        const double* yr = y + (size_t)r * cols;
+        for (int c = 0; c < cols; ++c) yb[c] = oracle_double_to_bf16(yr[c]);
+        oracle_quantize_blocks_e4m3(1, cols, ORACLE_PAYLOAD_BLOCK, yb, q, sc);
+        for (int c = 0; c < cols; ++c)
+            y_deq[(size_t)r * cols + c] = oracle_e4m3_decode(q[c]) * (double)sc[c / ORACLE_PAYLOAD_BLOCK];
+        if (codes) memcpy(codes + (size_t)r * cols, q, (size_t)cols);
+        if (scale) memcpy(scale + (size_t)r * nb, sc, (size_t)nb * sizeof(float));
+    }
+    free(yb); free(q); free(sc);
+}
+
 uint16_t oracle_double_to_bf16(double v) {
     if (isnan(v)) return 0x7FC0;
     if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
@@ -584,6 +613,7 @@ int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, cons
                                   sd + (size_t)slot * H, yd + (size_t)row * H);
         }
     }
+    oracle_payload_e4m3((int)n, H, yd, yd, NULL, NULL);  /* in place: each row read before it is written */
     for (int t = 0; t < T; ++t)
         oracle_shared_row_fp8(s, qx + (size_t)t * H, sx[t], qsg, ssg, qsu, ssu, qsd, ssd, ysh + (size_t)t * H);
     oracle_combine(s, T, yd, inv, w, ysh, out);

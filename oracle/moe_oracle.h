@@ -185,12 +185,27 @@ void oracle_swiglu_row_fp8(int H, int I, const uint8_t* qx, float sx, const uint
 void oracle_shared_row_fp8(const oracle_shape* s, const uint8_t* qx, float sx, const uint8_t* qsg, const float* ssg,
                            const uint8_t* qsu, const float* ssu, const uint8_t* qsd, const float* ssd, double* y);
 
+/* Block quantisation: each row is cut into blocks of `block` columns (the
+ * last one may be shorter) and each block is quantised as its own row by
+ * oracle_quantize_rows_e4m3: scale[r][b] = amax(|block|) / 448 in fp32 (1 for
+ * an all-zero block).  scale [rows, ceil(cols/block)]. */
+void oracle_quantize_blocks_e4m3(int rows, int cols, int block, const uint16_t* x_bf16, uint8_t* codes,
+                                 float* scale);
+
+/* The E4M3 combine payload (section 2.3: FP8 communication halves the combine
+ * bytes too).  An expert output row y (fp64) travels as its bf16 value (the
+ * bf16 layer's payload) quantised in blocks of ORACLE_PAYLOAD_BLOCK columns;
+ * y_deq = decode(code) * block scale, exact in fp64.  codes/scale may be NULL. */
+#define ORACLE_PAYLOAD_BLOCK 128
+void oracle_payload_e4m3(int rows, int cols, const double* y, double* y_deq, uint8_t* codes, float* scale);
+
 /* Whole layer in FP8: routing as oracle_moe_forward (bf16 router), every
  * token quantised once per row (its k dispatched copies carry the same codes
  * and scale), routed experts by oracle_swiglu_row_fp8 (qg/qu [S,I,H] with
- * scales [S*I], qd [S,H,I] with [S*H]), shared experts by
- * oracle_shared_row_fp8, combine as oracle_combine.  Returns the number of
- * invalid expert ids. */
+ * scales [S*I], qd [S,H,I] with [S*H]), their outputs carried back as the
+ * E4M3 payload of oracle_payload_e4m3, shared experts by
+ * oracle_shared_row_fp8 (local to the token, no payload), combine as
+ * oracle_combine.  Returns the number of invalid expert ids. */
 int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
                            const float* bias, const int32_t* replica_of, const uint8_t* qg, const float* sg,
                            const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd,

@@ -596,8 +596,63 @@ def test_shared_down_matrix_layout():
         assert torch.equal(m[:, 5 * j:5 * (j + 1)], sd[j])
 
 
+def _quantise_blocks_torch(rows_bf16, block):
+    """Block-wise E4M3 with torch: each run of `block` columns quantised as its own row."""
+    out = torch.empty(rows_bf16.shape, dtype=torch.float64)
+    for c0 in range(0, rows_bf16.shape[-1], block):
+        out[..., c0:c0 + block] = _quantise_torch(rows_bf16[..., c0:c0 + block])
+    return out
+
+
+def test_block_quantizer_matches_torch_per_block():
+    """Blocks of 128 columns with a shorter last block (300 = 128 + 128 + 44),
+    an all-zero block, and an outlier that sets one block's scale only."""
+    x = _bf16((6, 300), 1.5, 3, 21)
+    x[1, 128:256] = 0
+    x[2, 140] = 3008.0  # exact in bf16
+    codes, scale = oracle.quantize_blocks_e4m3(x, 128)
+    assert scale.shape == (6, 3)
+    xf = x.float()
+    for b, (c0, c1) in enumerate(((0, 128), (128, 256), (256, 300))):
+        amax = xf[:, c0:c1].abs().amax(-1)
+        want = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).numpy()
+        np.testing.assert_array_equal(scale[:, b], want)
+        q = (xf[:, c0:c1] / torch.from_numpy(want)[:, None]).to(torch.float8_e4m3fn)
+        assert np.array_equal(codes[:, c0:c1], q.view(torch.uint8).numpy())
+    assert scale[1, 1] == 1.0 and np.all(codes[1, 128:256] == 0)
+    assert scale[2, 1] == np.float32(3008.0) / np.float32(448.0) and scale[2, 0] != scale[2, 1]
+    # one block as wide as the row is the row quantiser
+    c_r, s_r = oracle.quantize_rows_e4m3(x)
+    c_b, s_b = oracle.quantize_blocks_e4m3(x, 300)
+    assert np.array_equal(c_b, c_r) and np.array_equal(s_b[:, 0], s_r)
+
+
+def test_payload_is_the_bf16_row_block_quantised():
+    """The E4M3 combine payload of an fp64 expert output: its bf16 rounding in
+    blocks of 128 columns; the dequantised row is code * block scale, within
+    the bf16 rounding plus half an E4M3 step of each element."""
+    rng = np.random.default_rng(31)
+    y = rng.normal(0.0, 0.7, (5, 300))
+    y[3, 260:] = 0.0
+    y[4, 5] = 90.0
+    deq, codes, scale = oracle.payload_e4m3(y)
+    yb = torch.from_numpy(oracle.bf16_round(y).view(np.int16)).view(torch.bfloat16)
+    c2, s2 = oracle.quantize_blocks_e4m3(yb, oracle.PAYLOAD_BLOCK)
+    assert np.array_equal(codes, c2) and np.array_equal(scale, s2)
+    blk = np.repeat(scale.astype(np.float64), oracle.PAYLOAD_BLOCK, axis=1)[:, :300]
+    np.testing.assert_array_equal(deq, _e4m3_values(codes).numpy() * blk)
+    np.testing.assert_array_equal(deq, _quantise_blocks_torch(yb, oracle.PAYLOAD_BLOCK).numpy())
+    ybf = yb.double().numpy()
+    normal = np.abs(ybf) >= 2.0 ** -6 * blk
+    err = np.abs(deq - ybf)
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(ybf[normal]) * 1.0000001)
+    assert np.all(err[~normal] <= 2.0 ** -10 * blk[~normal] * 1.0000001)
+    assert scale[4, 0] == np.float32(90.0) / np.float32(448.0) and scale[4, 1] < scale[4, 0]
+
+
 def test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors():
-    w = _tiny(top_k=3, n_shared=2, inter_shared=24, tokens=21)
+    # hidden 320: expert outputs travel back in 128-column payload blocks, the last one 64 wide
+    w = _tiny(top_k=3, n_shared=2, inter_shared=24, tokens=21, hidden=320)
     x, wr, _, wg, wu, wd, sg, su, sd = _tiny_inputs(w)
     q = oracle.quantize_layer_fp8(w, wg, wu, wd, sg, su, sd)
     r = oracle.moe_forward_fp8(w, x, wr, None, None, q)
@@ -620,7 +675,11 @@ def test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors():
     for e in range(w.n_experts):
         h = F.silu(F.linear(xq, G[e])) * F.linear(xq, U[e])
         y = F.linear(_quantise_torch(h.to(torch.bfloat16)), D[e])
-        ref += ((top == e).any(-1).double() * p[:, e])[:, None] * y
+        # the E4M3 combine payload; y rounded to bf16 once (the pinned bf16_round: torch's float64 -> bf16
+        # conversion rounds twice, through float32)
+        yb = torch.from_numpy(oracle.bf16_round(y.numpy()).view(np.int16)).view(torch.bfloat16)
+        yq = _quantise_blocks_torch(yb, oracle.PAYLOAD_BLOCK)
+        ref += ((top == e).any(-1).double() * p[:, e])[:, None] * yq
     hsh = torch.cat([F.silu(F.linear(xq, SG[j])) * F.linear(xq, SU[j]) for j in range(w.n_shared)], -1)
     ref += F.linear(_quantise_torch(hsh.to(torch.bfloat16)), SD)
     assert np.array_equal(np.sort(r["idx"], 1), np.sort(top.numpy(), 1))

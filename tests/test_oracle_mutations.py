@@ -49,6 +49,17 @@ MUTANTS = [
     ("fp8 down ignores the weight-row scale", "y[o] = acc * (double)sh * (double)sd[o];", "y[o] = acc * (double)sh;"),
     ("fp8 down reads its weights transposed", "dec[qd[(size_t)o * K + i]];",
      "dec[qd[(size_t)i * H + o]];"),
+    ("payload scale per row instead of per block",
+     "oracle_quantize_blocks_e4m3(1, cols, ORACLE_PAYLOAD_BLOCK, yb, q, sc);",
+     "oracle_quantize_blocks_e4m3(1, cols, cols, yb, q, sc);\n        for (int b = 1; b < nb; ++b) sc[b] = sc[0];"),
+    ("payload skipped in the E4M3 layer", "oracle_payload_e4m3((int)n, H, yd, yd, NULL, NULL);", "(void)n;"),
+    ("payload dequantised with the wrong block's scale",
+     "oracle_e4m3_decode(q[c]) * (double)sc[c / ORACLE_PAYLOAD_BLOCK];",
+     "oracle_e4m3_decode(q[c]) * (double)sc[(c / ORACLE_PAYLOAD_BLOCK + 1) % nb];"),
+    ("payload quantised from unrounded values",
+     "for (int c = 0; c < cols; ++c) yb[c] = oracle_double_to_bf16(yr[c]);",
+     "for (int c = 0; c < cols; ++c) { float f_ = (float)yr[c]; uint32_t b_; memcpy(&b_, &f_, 4); "
+     "yb[c] = (uint16_t)(b_ >> 16); }"),
     ("bf16 rounding truncates", "const double r = rint(v / step) * step;", "const double r = trunc(v / step) * step;"),
     ("home slot ignores the replica slots", "return (e / epb) * spb + (e % epb);", "return e;"),
     ("replica used by even tokens", "replica_of[e] >= 0 && (t % 2) == 1", "replica_of[e] >= 0 && (t % 2) == 0"),
@@ -99,6 +110,8 @@ PINS = [
     pins.test_fp8_gate_up_row_reduces_to_bf16_on_exact_values,
     pins.test_fp8_expert_row_is_gate_up_then_bf16_row_quantised_down,
     pins.test_fp8_layer_matches_dense_bruteforce_on_dequantised_tensors,
+    pins.test_block_quantizer_matches_torch_per_block,
+    pins.test_payload_is_the_bf16_row_block_quantised,
     pins.test_eplb_window_hand_case,
     pins.test_eplb_window_matches_histograms_of_recent_batches,
 ]
