@@ -170,14 +170,16 @@ def routing_stats(w, counts_np, blocks_np, replica_of=None):
 def layer_bytes_flops(w, counts_np, fp8=False):
     """Algorithmic bytes and flops of one layer pass (touched expert weights read once).
 
-    fp8: expert weights and the dispatch payload are one byte per element.
+    fp8: expert weights and both payloads are one byte per element (plus the
+    combine payload's fp32 scale per 128-column block).
     """
     H, I, E, k, T = w.hidden, w.inter, w.n_experts, w.top_k, w.tokens
     gb = 1 if fp8 else 2  # bytes per expert weight and per dispatched element
     touched = int((counts_np[:w.n_slots] > 0).sum())
     expert_bytes = 3 * H * I * gb
     shared_bytes = w.n_shared * 3 * H * w.inter_shared * gb
-    act = T * H * 2 + 2 * T * k * H * gb + 2 * T * k * H * 2 + T * H * 2
+    y_row = H + 4 * ((H + 127) // 128) if fp8 else 2 * H  # combine payload bytes per assignment
+    act = T * H * 2 + 2 * T * k * H * gb + 2 * T * k * y_row + T * H * 2
     B = touched * expert_bytes + shared_bytes + E * H * 2 + act
     F = 6 * H * I * T * k + 6 * H * w.inter_shared * w.n_shared * T + 2 * T * H * E
     # gate/up launch: gate+up weights of touched slots and shared, x_disp + x read, h written
@@ -188,16 +190,62 @@ def layer_bytes_flops(w, counts_np, fp8=False):
 
 # ------------------------------------------------------------------------------ our arm
 
-def run_ours(args, rank, world, local_rank):
-    import moe_expert_layer_06_gb300 as m
-    if rank == 0:
-        m.build_library()
-    if world > 1:
-        torch.distributed.barrier()
-    m.build_library()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    w = mi.WORKLOADS[args.config]
+# workloads timed after the headline one, in the same run and with the same step count
+EXTRA_CONFIGS = ("decode_t256_skew", "prefill_t4096", "redundant_t1024")
+
+
+class DeviceWeights:
+    """Expert weights on the device, generated once per expert shape and shared by
+    the workloads of that shape (a replica slot is a byte copy of its expert)."""
+
+    def __init__(self, m, dev):
+        self.m, self.dev = m, dev
+        self.key, self.base, self.q = None, None, None
+
+    def _base(self, w):
+        key = (w.hidden, w.inter, w.n_experts, w.n_shared, w.inter_shared, w.seed)
+        if key != self.key:  # one expert shape resident at a time
+            self.key, self.base, self.q = None, None, None
+            torch.cuda.empty_cache()
+            base = w.with_(n_slots=w.n_experts)
+            wg, wu, wd = mi.stacked_expert_weights(base, device=self.dev)
+            sg, su, sd = mi.stacked_shared_weights(base, device=self.dev)
+            mi.clear_cache()
+            self.key, self.base = key, (wg, wu, wd, sg, su, sd)
+        return self.base
+
+    def bf16(self, w, rep):
+        wg, wu, wd, sg, su, sd = self._base(w)
+        if w.n_slots > w.n_experts:
+            se = torch.from_numpy(mi.slot_experts(w, rep)).to(self.dev)
+            wg, wu, wd = (t.index_select(0, se) for t in (wg, wu, wd))
+        return wg, wu, wd, sg, su, sd
+
+    def fp8(self, w, rep):
+        """E4M3 codes and one scale per output row of every expert matrix; the shared
+        experts' down matrices as one [H, n_sh*I_sh] matrix (their outputs are summed)."""
+        m, dev = self.m, self.dev
+        wg, wu, wd, sg, su, sd = self._base(w)
+        if self.q is None:
+            def quant(t):
+                q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
+                sc = torch.empty(t.shape[:-1], dtype=torch.float32, device=dev)
+                m.moe_quantize_rows_fp8(t.view(-1, t.shape[-1]), q, sc)
+                return q, sc
+            self.q = quant(wg) + quant(wu) + quant(wd) + quant(sg) + quant(su) + \
+                quant(sd.permute(1, 0, 2).reshape(w.hidden, -1).contiguous())
+            torch.cuda.synchronize(dev)
+        q = list(self.q)
+        if w.n_slots > w.n_experts:
+            se = torch.from_numpy(mi.slot_experts(w, rep)).to(dev)
+            q[:6] = [t.index_select(0, se) for t in q[:6]]
+        return tuple(q)
+
+
+def measure(m, args, w, dev, rank, world, local_rank, weights, with_cpu_baseline):
+    """Time one workload: K device-timed steps (stage kernels through the C ABI),
+    then K end-to-end steps through moe_forward with host copies.  Returns the
+    JSON fields of that workload (rank 0) or None."""
     T = w.tokens
     rep = None
     if w.n_slots > w.n_experts:
@@ -206,22 +254,11 @@ def run_ours(args, rank, world, local_rank):
     wr = mi.router_weight(w, device=dev)
     b = mi.router_bias(w)
     bias = torch.from_numpy(b).to(dev) if b is not None else None
-    wg, wu, wd = mi.stacked_expert_weights(w, rep, device=dev)
-    sg, su, sd = mi.stacked_shared_weights(w, device=dev)
-    mi.clear_cache()
     fp8 = bool(args.fp8)
-    if fp8:  # E4M3 expert weights with one scale per output row (the bf16 copies are dropped)
-        def quant(t):
-            q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
-            sc = torch.empty(t.numel() // t.shape[-1], dtype=torch.float32, device=dev)
-            m.moe_quantize_rows_fp8(t.view(-1, t.shape[-1]), q, sc)
-            return q, sc
-        (qg, s_g), (qu, s_u), (qd, s_d) = quant(wg), quant(wu), quant(wd)
-        (qsg, s_sg), (qsu, s_su) = quant(sg), quant(su)
-        # the shared experts' down matrices as one [H, n_sh*I_sh] matrix (their outputs are summed)
-        qsd, s_sd = quant(sd.permute(1, 0, 2).reshape(w.hidden, -1).contiguous())
-        del wg, wu, wd, sg, su, sd
-        torch.cuda.synchronize(dev)
+    if fp8:
+        qg, s_g, qu, s_u, qd, s_d, qsg, s_sg, qsu, s_su, qsd, s_sd = weights.fp8(w, rep)
+    else:
+        wg, wu, wd, sg, su, sd = weights.bf16(w, rep)
     repd = torch.from_numpy(rep).to(dev) if rep is not None else None
     torch.cuda.empty_cache()
 
@@ -246,12 +283,15 @@ def run_ours(args, rank, world, local_rank):
         h8s = torch.empty(n, dtype=torch.float32, device=dev)
         hs8 = torch.empty((T, w.n_shared * w.inter_shared), dtype=torch.uint8, device=dev)
         hs8s = torch.empty(T, dtype=torch.float32, device=dev)
+        y8 = torch.empty((n, H), dtype=torch.uint8, device=dev)
+        y8s = torch.empty((n, (H + m.MOE_PAYLOAD_BLOCK - 1) // m.MOE_PAYLOAD_BLOCK), dtype=torch.float32, device=dev)
     h = torch.empty((n, I), dtype=torch.bfloat16, device=dev)
     hs = torch.empty((T, w.n_shared * w.inter_shared), dtype=torch.bfloat16, device=dev)
     y = torch.empty((n, H), dtype=torch.bfloat16, device=dev)
     ysh = torch.empty((T, H), dtype=torch.float32, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     rws = torch.empty(max(16, m.moe_route_workspace_size(w, T)), dtype=torch.uint8, device=dev)
+    dws = torch.empty(max(16, m.moe_dispatch_workspace_size(w, T)), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     ffn_mode = {"auto": m.MOE_FFN_AUTO, "decode": m.MOE_FFN_DECODE, "prefill": m.MOE_FFN_PREFILL}[args.ffn_mode]
@@ -259,16 +299,18 @@ def run_ours(args, rank, world, local_rank):
     if args.route_groups:
         groups = tuple(int(v) for v in args.route_groups.split(":"))
 
-    def step(ev=None):
+    def step(ev=None, st=None):
         if groups:
             m.moe_route_grouped(w, T, groups[0], groups[1], x, wr, bias, None, None, idx, tw, rws)
         else:
             m.moe_route(w, T, x, wr, bias, None, None, idx, tw, rws)
+        if st is not None:
+            st[0].record(stream)
         if fp8:
             m.moe_dispatch_fp8(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x8, xs8, x_disp8,
-                               xds8)
+                               xds8, ws=dws)
         else:
-            m.moe_dispatch(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x_disp)
+            m.moe_dispatch(w, T, x, idx, repd, slot_of, counts, blocks, offsets, perm, inv, x_disp, ws=dws)
         if ev is not None:
             ev[0].record(stream)
         if fp8:
@@ -282,10 +324,16 @@ def run_ours(args, rank, world, local_rank):
             m.moe_quantize_rows_fp8(h, h8, h8s)
             if w.n_shared:
                 m.moe_quantize_rows_fp8(hs, hs8, hs8s)
-            m.moe_expert_down_fp8(w, T, h8, h8s, hs8, hs8s, offsets, qd, s_d, qsd, s_sd, y, ysh, mode=ffn_mode)
+            m.moe_expert_down_fp8_payload(w, T, h8, h8s, hs8, hs8s, offsets, qd, s_d, qsd, s_sd, y8, y8s, ysh,
+                                          mode=ffn_mode)
         else:
             m.moe_expert_down(w, T, h, hs, offsets, wd, sd, y, ysh, mode=ffn_mode)
-        m.moe_combine(w, T, y, inv, tw, ysh, out)
+        if st is not None:
+            st[1].record(stream)
+        if fp8:
+            m.moe_combine_fp8(w, T, y8, y8s, inv, tw, ysh, out)
+        else:
+            m.moe_combine(w, T, y, inv, tw, ysh, out)
 
     # router GEMM + top-k, index pass (three launches in chunks for large batches), scatter
     # (E4M3: + token quantisation), gate/up, (E4M3: + intermediate quantisation), down, combine
@@ -310,9 +358,11 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    sts = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)] if args.stage_times else [None] * args.steps
     t0.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step(evs[i], sts[i])
     t1.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -395,19 +445,11 @@ def run_ours(args, rank, world, local_rank):
     ms_step = elapsed_ms / args.steps
     t_roof_ms = max(bf["bytes"] / (hbm * 1e9), bf["flops"] / (tf_sus * 1e12)) * 1e3
     achieved = bf["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
+    tflops = bf["flops"] / (ms_step * 1e-3) / 1e12
     res = {
-        "metric": METRIC,
         "value": round(job_tokens_per_s(T, world, ms_step), 1),
         "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "e4m3" if fp8 else "bf16",
-        "data": "synthetic (seeded counter-based generator; random-init DeepSeek-V3 MoE layer weights)",
         "config": {
             "workload": w.name, "description": w.description, "tokens": T, "hidden": H, "inter": I,
             "n_experts": E, "top_k": k, "n_shared": w.n_shared, "n_slots": S,
@@ -415,8 +457,9 @@ def run_ours(args, rank, world, local_rank):
             "l2": "inputs larger than L2: each step streams %.1f GB of touched expert weights" % (bf["bytes"] / 1e9),
             "parallelism": "replica x%d (independent layer per GPU)" % world,
             "routing": ("group-limited: %d groups, keep %d" % groups) if groups else "top-%d of all experts" % k,
-            "precision": ("E4M3 expert weights (gate, up, down; shared included), dispatch payload and SwiGLU "
-                          "intermediate, per-row scales, fp32 accumulate; bf16 router, expert outputs and combine")
+            "precision": ("E4M3 expert weights (gate, up, down; shared included), dispatch payload, SwiGLU "
+                          "intermediate (per-row scales) and combine payload (one scale per 128-column block), "
+                          "fp32 accumulate; bf16 router and layer output")
             if fp8 else "bf16 weights and activations, fp32 accumulate",
         },
         "us_per_layer": round(ms_step * 1e3, 2),
@@ -424,6 +467,9 @@ def run_ours(args, rank, world, local_rank):
             "bound": "hbm" if bf["bytes"] / (hbm * 1e9) >= bf["flops"] / (tf_sus * 1e12) else "tensor",
             "algorithmic_bytes": bf["bytes"], "flops": bf["flops"], "t_roof_us": round(t_roof_ms * 1e3, 2),
             "frac": round(t_roof_ms / ms_step, 4), "peaks": src,
+            "achieved_gbs": round(bf["bytes"] / (ms_step * 1e-3) / 1e9, 1),
+            "achieved_tflops": round(tflops, 2),
+            "tensor_frac_of_sustained_bf16": round(tflops / tf_sus, 4),
         },
         "roofline": {
             "kernel": ("grouped_gemm_kernel<gate_up_e4m3> (moe_expert_gate_up_fp8)" if fp8
@@ -452,8 +498,54 @@ def run_ours(args, rank, world, local_rank):
         "routing_stats": routing_stats(w, cnt, blocks.cpu().numpy(), rep),
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if args.stage_times:  # per-stage means; the extra events sit between launches of the step
+        res["stage_us"] = {
+            "dispatch": round(sum(s_[0].elapsed_time(e_[0]) for s_, e_ in zip(sts, evs)) / args.steps * 1e3, 2),
+            "gate_up": round(gu_ms * 1e3, 2),
+            "down": round(sum(e_[1].elapsed_time(s_[1]) for s_, e_ in zip(sts, evs)) / args.steps * 1e3, 2),
+        }
+    if with_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, dev, args.cpu_sample)
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import moe_expert_layer_06_gb300 as m
+    if rank == 0:
+        m.build_library()
+    if world > 1:
+        torch.distributed.barrier()
+    m.build_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    weights = DeviceWeights(m, dev)
+    w = mi.WORKLOADS[args.config]
+    main = measure(m, args, w, dev, rank, world, local_rank, weights, world == 1 and not args.no_cpu_baseline)
+    extra = {}
+    if args.config == DEFAULT_CONFIG and not args.no_extra_configs and not args.route_groups:
+        for name in EXTRA_CONFIGS:
+            r = measure(m, args, mi.WORKLOADS[name], dev, rank, world, local_rank, weights, False)
+            if r is not None:
+                extra[name] = r
+    if rank != 0:
+        return None
+    res = {
+        "metric": METRIC,
+        "value": main["value"],
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": main["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3" if args.fp8 else "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init DeepSeek-V3 MoE layer weights)",
+    }
+    res.update({k_: v for k_, v in main.items() if k_ not in ("value", "unit", "ms_per_step")})
+    if extra:
+        res["configs"] = extra
     return res
 
 
@@ -663,6 +755,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage-times", action="store_true",
+                    help="also record CUDA events around the dispatch and the down projection of every step")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time the headline workload only (by default the decode line also times "
+                         + ", ".join(EXTRA_CONFIGS) + ")")
     ap.add_argument("--route-groups", default="", help="G:Gk group-limited routing (timed region only)")
     ap.add_argument("--eplb", action="store_true", help="time the online EPLB loop instead (own JSON line)")
     ap.add_argument("--fp8", action="store_true", help="E4M3 expert weights and dispatch payload")

@@ -343,10 +343,22 @@ MOE_API int moe_expert_ffn_noalloc(const moe_shape_t* shape, int T, const void* 
  * ssd [H].  y_disp[row, o] = bf16(h_scale[row] * sd[slot*H+o] * sum_i
  * h8*qd); y_shared[t, o] = hs_scale[t] * ssd[o] * sum_i hs8*qsd in fp32.
  * inter % 16 == 0 and n_sh*I_sh % 16 == 0.
+ * moe_expert_down_fp8_payload: moe_expert_down_fp8 whose routed outputs
+ * leave as the E4M3 combine payload (section 2.3 halves the combine volume
+ * too): each row's bf16 value (the y_disp of moe_expert_down_fp8) is cut into
+ * blocks of MOE_PAYLOAD_BLOCK columns (the last one shorter when hidden is
+ * not a multiple), each block quantised with its own fp32 scale as above:
+ * y_disp8 [T*k, H] u8 codes, y_disp_scale [T*k, ceil(H/MOE_PAYLOAD_BLOCK)].
+ * Per token the payload is k*H bytes plus k*ceil(H/128)*4 bytes of scales
+ * (59,136 B at k=8, H=7168).  y_shared as moe_expert_down_fp8 (fp32, local).
+ * moe_combine_fp8: moe_combine on that payload; an expert output element is
+ * decode(code) * the scale of its block, in fp32.  hidden % 16 == 0.
  * moe_forward_fp8: route (bf16 router), moe_dispatch_fp8,
  * moe_expert_gate_up_fp8, the two intermediate quantisations,
- * moe_expert_down_fp8, moe_combine, intermediates in a workspace of
- * moe_workspace_size_fp8() bytes.  Every expert matrix is E4M3. */
+ * moe_expert_down_fp8_payload, moe_combine_fp8, intermediates in a workspace
+ * of moe_workspace_size_fp8() bytes.  Every expert matrix is E4M3, and so are
+ * the dispatch and the combine payloads. */
+#define MOE_PAYLOAD_BLOCK 128
 MOE_API int moe_quantize_rows_fp8(int rows, int cols, const void* x, uint8_t* codes, float* scale, void* stream);
 MOE_API int moe_dispatch_fp8(const moe_shape_t* shape, int T, const void* x, const int32_t* topk_idx,
                              const int32_t* replica_of, int32_t* slot_of, int32_t* counts, int32_t* block_counts,
@@ -362,6 +374,14 @@ MOE_API int moe_expert_down_fp8(const moe_shape_t* shape, int T, const uint8_t* 
                                 const uint8_t* hs8, const float* hs_scale, const int32_t* offsets, const uint8_t* qd,
                                 const float* sd, const uint8_t* qsd, const float* ssd, void* y_disp, float* y_shared,
                                 int mode, void* stream);
+MOE_API int moe_expert_down_fp8_payload(const moe_shape_t* shape, int T, const uint8_t* h8, const float* h_scale,
+                                        const uint8_t* hs8, const float* hs_scale, const int32_t* offsets,
+                                        const uint8_t* qd, const float* sd, const uint8_t* qsd, const float* ssd,
+                                        uint8_t* y_disp8, float* y_disp_scale, float* y_shared, int mode,
+                                        void* stream);
+MOE_API int moe_combine_fp8(const moe_shape_t* shape, int T, const uint8_t* y_disp8, const float* y_disp_scale,
+                            const int32_t* inv_perm, const float* topk_w, const float* y_shared, void* out,
+                            void* stream);
 MOE_API size_t moe_workspace_size_fp8(const moe_shape_t* shape, int T);
 MOE_API int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
                             const int32_t* replica_of, const uint8_t* qg, const float* sg, const uint8_t* qu,

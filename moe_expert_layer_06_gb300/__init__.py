@@ -39,7 +39,11 @@ EXPORTS = (
     "moe_eplb_window_bytes", "moe_eplb_window_reset", "moe_eplb_window_push", "moe_eplb_stable_table",
     "moe_eplb_copy_replicas", "moe_quantize_rows_fp8", "moe_dispatch_fp8", "moe_expert_gate_up_fp8",
     "moe_workspace_size_fp8", "moe_forward_fp8", "moe_expert_down_fp8", "moe_dispatch_workspace_size",
+    "moe_expert_down_fp8_payload", "moe_combine_fp8",
 )
+
+# columns per scale of the E4M3 combine payload (MOE_PAYLOAD_BLOCK in include/moe.h)
+MOE_PAYLOAD_BLOCK = 128
 
 # capacity of the fixed scratch of moe_expert_ffn_noalloc (include/moe.h)
 MOE_FFN_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -96,6 +100,8 @@ _SIG = {
     "moe_expert_gate_up_fp8": (_I, [_P, _I] + [_P] * 15 + [_I, _P]),
     "moe_workspace_size_fp8": (_Z, [_P, _I]),
     "moe_expert_down_fp8": (_I, [_P, _I] + [_P] * 11 + [_I, _P]),
+    "moe_expert_down_fp8_payload": (_I, [_P, _I] + [_P] * 12 + [_I, _P]),
+    "moe_combine_fp8": (_I, [_P, _I] + [_P] * 7),
     "moe_forward_fp8": (_I, [_P, _I] + [_P] * 21 + [_I, _P, _Z, _P]),
     "moe_workspace_size": (_Z, [_P, _I]),
     "moe_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
@@ -349,6 +355,18 @@ def moe_expert_down_fp8(shape, T, h8, h_scale, hs8, hs_scale, offsets, qd, sd, q
     _check(lib().moe_expert_down_fp8(_shape(shape), T, _ptr(h8), _ptr(h_scale), _ptr(hs8), _ptr(hs_scale),
                                      _ptr(offsets), _ptr(qd), _ptr(sd), _ptr(qsd), _ptr(ssd), _ptr(y_disp),
                                      _ptr(y_shared), mode, _stream(stream)))
+
+
+def moe_expert_down_fp8_payload(shape, T, h8, h_scale, hs8, hs_scale, offsets, qd, sd, qsd, ssd, y_disp8,
+                                y_disp_scale, y_shared, mode=MOE_FFN_AUTO, stream=None):
+    _check(lib().moe_expert_down_fp8_payload(_shape(shape), T, _ptr(h8), _ptr(h_scale), _ptr(hs8), _ptr(hs_scale),
+                                             _ptr(offsets), _ptr(qd), _ptr(sd), _ptr(qsd), _ptr(ssd), _ptr(y_disp8),
+                                             _ptr(y_disp_scale), _ptr(y_shared), mode, _stream(stream)))
+
+
+def moe_combine_fp8(shape, T, y_disp8, y_disp_scale, inv_perm, topk_w, y_shared, out, stream=None):
+    _check(lib().moe_combine_fp8(_shape(shape), T, _ptr(y_disp8), _ptr(y_disp_scale), _ptr(inv_perm), _ptr(topk_w),
+                                 _ptr(y_shared), _ptr(out), _stream(stream)))
 
 
 def moe_workspace_size_fp8(shape, T: int) -> int:

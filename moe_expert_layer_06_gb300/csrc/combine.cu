@@ -4,7 +4,12 @@
 // their token (here: a gather through inv_perm) and
 //   out[t] = sum_{j<k} softmax(logits)[idx_j] * expert_out_j + shared_out[t],
 // accumulated in fp32 in ascending j, then the shared expert output, rounded
-// once to bf16.  8 bf16 (16 bytes) per thread per step.
+// once to bf16.  8 bf16 (16 bytes) per thread per step.  With the E4M3
+// combine payload (section 2.3: FP8 communication) each expert output element
+// is its code times the fp32 scale of its 128-column block.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "kernels.h"
 
 namespace moe {
@@ -81,7 +86,91 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     }
 }
 
+// E4M3 payload: 8 codes (8 bytes) per thread per step, dequantised with the
+// scale of their 128-column block (8 | 128, so a vector never straddles two
+// blocks); otherwise as combine_kernel.
+__global__ void __launch_bounds__(256) combine_fp8_kernel(const uint2* __restrict__ y8,
+                                                          const float* __restrict__ y_scale,
+                                                          const int32_t* __restrict__ inv_perm,
+                                                          const float* __restrict__ topk_w,
+                                                          const float4* __restrict__ y_shared, int T, int k,
+                                                          int vec_per_row, int n_blk, uint4* __restrict__ out) {
+    pdl_begin();
+    const size_t total = (size_t)T * vec_per_row;
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(idx / vec_per_row);
+        const int c = (int)(idx - (size_t)t * vec_per_row);
+        const int blk = (c * 8) / kPayloadBlock;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+        if (y_shared) {
+            s0 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2);
+            s1 = __ldg(y_shared + ((size_t)t * vec_per_row + c) * 2 + 1);
+        }
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            int row[8];
+            float w[8], sc[8];
+            uint2 yv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (j0 + u < k) {
+                    row[u] = __ldg(inv_perm + (size_t)t * k + j0 + u);
+                    w[u] = __ldg(topk_w + (size_t)t * k + j0 + u);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (j0 + u < k) {
+                    yv[u] = __ldg(y8 + (size_t)row[u] * vec_per_row + c);
+                    sc[u] = __ldg(y_scale + (size_t)row[u] * n_blk + blk);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (j0 + u < k) {
+                    const uint32_t wd[2] = {yv[u].x, yv[u].y};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+                            (__nv_fp8x2_storage_t)((wd[h >> 1] >> ((h & 1) * 16)) & 0xffffu), __NV_E4M3);
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                        acc[2 * h] = fmaf(w[u], f.x * sc[u], acc[2 * h]);
+                        acc[2 * h + 1] = fmaf(w[u], f.y * sc[u], acc[2 * h + 1]);
+                    }
+                }
+            }
+        }
+        if (y_shared) {
+            acc[0] += s0.x; acc[1] += s0.y; acc[2] += s0.z; acc[3] += s0.w;
+            acc[4] += s1.x; acc[5] += s1.y; acc[6] += s1.z; acc[7] += s1.w;
+        }
+        uint4 o;
+        o.x = pack2(acc[0], acc[1]);
+        o.y = pack2(acc[2], acc[3]);
+        o.z = pack2(acc[4], acc[5]);
+        o.w = pack2(acc[6], acc[7]);
+        out[idx] = o;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_fp8(const uint8_t* y8, const float* y_scale, const int32_t* inv_perm, const float* topk_w,
+                               const float* y_shared, int T, int k, int hidden, uint16_t* out, cudaStream_t stream) {
+    const int vpr = hidden / 8;
+    const size_t total = (size_t)T * vpr;
+    if (total == 0) return cudaSuccess;
+    size_t blocks = (total + 255) / 256;
+    const size_t cap = (size_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(combine_fp8_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                      reinterpret_cast<const uint2*>(y8), y_scale, inv_perm, topk_w,
+                      reinterpret_cast<const float4*>(y_shared), T, k, vpr, (hidden + kPayloadBlock - 1) / kPayloadBlock,
+                      reinterpret_cast<uint4*>(out));
+}
 
 cudaError_t launch_combine(const uint16_t* y_disp, const int32_t* inv_perm, const float* topk_w,
                            const float* y_shared, int T, int k, int hidden, uint16_t* out,

@@ -8,40 +8,11 @@
 // with saturation; the value is code * scale.
 #include <cuda_fp8.h>
 
+#include "e4m3.cuh"
 #include "kernels.h"
 
 namespace moe {
 namespace {
-
-// Row divisor: x / s correctly rounded (round to nearest even), as the
-// quantisation rule defines it.  For s >= 2^-96 the quotient comes from the
-// reciprocal r = RN(1/s) and one correction with the exact FMA residual:
-// q0 = RN(x r), e = x - q0 s (exact), q = RN(q0 + e r).  By Markstein's
-// theorem (a quotient within one ulp, corrected once with a reciprocal within
-// half an ulp, is the correctly rounded quotient, barring underflow and
-// overflow) this is RN(x / s); here |x| <= 448 s, so nothing overflows, and an
-// underflowing quotient is far below 2^-10, where every E4M3 code is a zero.
-// Smaller scales divide with __fdiv_rn.
-struct RowDiv {
-    float s, r;
-    bool fast;
-};
-
-__device__ __forceinline__ RowDiv row_div(float s) {
-    RowDiv d;
-    d.s = s;
-    d.r = __frcp_rn(s);
-    d.fast = s >= 0x1p-96f;
-    return d;
-}
-
-template <bool FAST>
-__device__ __forceinline__ float div_rn(const RowDiv& d, float x) {
-    if (!FAST) return __fdiv_rn(x, d.s);
-    const float q0 = x * d.r;
-    const float e = fmaf(-q0, d.s, x);
-    return fmaf(e, d.r, q0);
-}
 
 // E4M3 codes of 8 bf16 values (one 16-byte vector) at a row's scale, packed
 // into 8 bytes in element order (two values per conversion).
@@ -68,8 +39,6 @@ __device__ __forceinline__ float amax8(const uint4 q, float m) {
     }
     return m;
 }
-
-__device__ __forceinline__ float row_scale(float amax) { return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f; }
 
 // Single pass: a row is spread over tpr threads (a multiple of 32), each
 // holding up to kVpt 16-byte vectors in registers: load, amax over the row

@@ -26,6 +26,9 @@
 //   warps 2..17 epilogue: tcgen05.ld -> SwiGLU / convert -> global stores
 // Every mbarrier wait is bounded; on expiry the kernel raises the status word,
 // drains its own copies and MMAs (bounded) and frees its TMEM.
+#include <cuda_fp8.h>
+
+#include "e4m3.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -53,8 +56,9 @@ struct Item {
 // token-chunk byte.
 template <int MODE>
 struct Traits {
-    static constexpr bool kF8 = (MODE == kGateUpF8 || MODE == kDownF8);  // E4M3 operands
-    static constexpr bool kDownLike = (MODE == kDown || MODE == kDownF8);
+    static constexpr bool kF8 = (MODE == kGateUpF8 || MODE == kDownF8 || MODE == kDownF8Q);  // E4M3 operands
+    static constexpr bool kDownLike = (MODE == kDown || MODE == kDownF8 || MODE == kDownF8Q);
+    static constexpr bool kDownF8Like = (MODE == kDownF8 || MODE == kDownF8Q);
     static constexpr bool kGateUpLike = (MODE == kGateUp || MODE == kGateUpF8);
     static constexpr int NA = (MODE == kRouter) ? 1 : 2;
     static constexpr int kRowsPerItem = kDownLike ? 256 : 128;
@@ -78,7 +82,12 @@ struct Config {
     static constexpr int kTmemCols = pow2_at_least(kNumAcc * kAccCols);
     static constexpr int kBarBytes = (2 * STAGES + 2 * kNumAcc + 1) * 8;
     static constexpr int kTableBytes = (kMaxSlots + 4) * 4;
-    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + 16 + kTableBytes;
+    // column groups of 16 tokens one epilogue warp drains per item
+    static constexpr int kMaxG = (BN / 16 + kEpiWarps / 4 - 1) / (kEpiWarps / 4);
+    // kDownF8Q: per-warp column maxima exchanged by the four warps that share columns
+    // (two mbarriers per group of four warps, then the maxima)
+    static constexpr int kXchgBytes = MODE == kDownF8Q ? 64 + (kEpiWarps / 4) * 4 * kMaxG * 2 * 16 * 4 : 0;
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kBarBytes + 16 + kTableBytes + kXchgBytes;
     static_assert(kTmemCols <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory overflow");
     static_assert(BN <= 15 * 16, "token chunk must be at most 15 groups of 16 rows");
@@ -174,6 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     Table tb{reinterpret_cast<int*>(tmem_slot + 4)};
+    // kDownF8Q exchange: xfull[p] / xfree[p] (four warps arrive on each), then the maxima
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tmem_slot + 4) + C::kTableBytes);
+    float* xchg = reinterpret_cast<float*>(xbar + 8);
+    (void)xchg;
     constexpr int RPI = Traits<MODE>::kRowsPerItem;
 
     const int warp = threadIdx.x >> 5;
@@ -191,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             mbar_init(smem_u32(&tempty[s]), kEpiWarps);
         }
         mbar_init(smem_u32(mma_done), 1);
+        if (MODE == kDownF8Q)
+            for (int p = 0; p < 8; ++p) mbar_init(smem_u32(&xbar[p]), 4);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&a.a0);
@@ -385,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int part = ew >> 2;         // column groups part, part+4, ...
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t xph = 0;  // kDownF8Q: exchanges done by this warp
         bool ok = true;
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
@@ -402,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             if (Traits<MODE>::kGateUpLike) {
                 // SwiGLU per column group into packed bf16 registers, then free the
                 // accumulator (the next item's MMAs may start) and store
-                constexpr int kMaxG = (BN / 16 + kEpiWarps / 4 - 1) / (kEpiWarps / 4);
+                constexpr int kMaxG = C::kMaxG;
                 uint32_t hp[kMaxG][8];
                 const float* sa0 = nullptr;
                 const float* sa1 = nullptr;
@@ -471,6 +487,122 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 continue;
             }
+            if (MODE == kDownF8Q && !it.shared) {
+                // Routed rows leave as the E4M3 payload: block = 128 output rows (one TMEM
+                // half), one scale per (token, block).  The four warps that drain these
+                // columns hold 32 rows of every block each.  Pass 1: bf16 y, warp maxima
+                // of |y| per column into shared memory; pass 2 (after all four have
+                // written): reload, the block scale of each column, codes, stores.  The
+                // accumulator is held through both passes: the item's outputs do not fit
+                // the 96 registers a thread has at 18 warps (with 10 warps and 168
+                // registers the epilogue took longer than the items it overlapped).
+                constexpr int kMaxG = C::kMaxG;
+                const float* sbp = a.b_scale + it.row0;
+                const float* swp = a.a0_scale + (size_t)it.z * a.m_routed;
+                float* xw = xchg + (size_t)(part * 4 + q) * kMaxG * 2 * 16;
+                const float* xp = xchg + (size_t)part * 4 * kMaxG * 2 * 16;
+                const uint32_t xfull = smem_u32(&xbar[part]), xfree = smem_u32(&xbar[4 + part]);
+                // bf16 value of accumulator column group g, half hh of this lane's row
+                auto load_y = [&](int g, int hh, uint32_t (&yb)[8]) {
+                    float v[16];
+                    tmem_ld16(tl + hh * BN + g * 16, v);
+                    tmem_ld_wait();
+                    const int row = mrow + hh * 128;
+                    const float sw = row < mlim ? __ldg(swp + row) : 0.0f;  // rows past H are 0
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const int col = g * 16 + j;
+                        const float s0 = col < it.nrows ? __ldg(sbp + col) : 0.0f;
+                        const float s1 = col + 1 < it.nrows ? __ldg(sbp + col + 1) : 0.0f;
+                        const __nv_bfloat162 p2 = __floats2bfloat162_rn(v[j] * (sw * s0), v[j + 1] * (sw * s1));
+                        yb[j >> 1] = *reinterpret_cast<const uint32_t*>(&p2);
+                    }
+                };
+                // the four warps have read the previous item's maxima
+                if (xph > 0 && !mbar_wait(xfree, (xph - 1) & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll 1
+                for (int gi = 0; gi < kMaxG; ++gi) {
+                    const int g = part + gi * (kEpiWarps / 4);
+                    if (g >= nb) break;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (it.m0 + hh * 128 >= mlim) break;  // a half past the last output row: no block
+                        uint32_t yb[8];
+                        load_y(g, hh, yb);
+                        float mine = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint32_t mx = __reduce_max_sync(0xffffffffu, (yb[j >> 1] >> ((j & 1) * 16)) & 0x7fffu);
+                            if (lane == j) mine = __uint_as_float(mx << 16);
+                        }
+                        if (lane < 16) xw[(gi * 2 + hh) * 16 + lane] = mine;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xfull);
+                if (!mbar_wait(xfull, xph & 1, limit)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll 1
+                for (int gi = 0; gi < kMaxG; ++gi) {
+                    const int g = part + gi * (kEpiWarps / 4);
+                    if (g >= nb) break;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (it.m0 + hh * 128 >= mlim) break;
+                        const int row = mrow + hh * 128;
+                        const int blk = (it.m0 >> 7) + hh;
+                        // lane l < 16: scale of column l's block from the four warps' maxima
+                        const int o = (gi * 2 + hh) * 16 + (lane & 15);
+                        const float amax = fmaxf(fmaxf(xp[o], xp[kMaxG * 32 + o]),
+                                                 fmaxf(xp[2 * kMaxG * 32 + o], xp[3 * kMaxG * 32 + o]));
+                        const float sl = row_scale(amax);
+                        const int col_l = g * 16 + lane;
+                        if (q == 0 && lane < 16 && col_l < it.nrows)
+                            a.out8_scale[(size_t)(it.row0 + col_l) * a.n_blk + blk] = sl;
+                        const RowDiv dl = row_div(sl);
+                        uint32_t yb[8];
+                        load_y(g, hh, yb);
+                        uint8_t* dst8 = a.out8 + row;
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            float qv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                RowDiv d;
+                                d.s = __shfl_sync(0xffffffffu, dl.s, j + u);
+                                d.r = __shfl_sync(0xffffffffu, dl.r, j + u);
+                                d.fast = d.s >= 0x1p-96f;
+                                const float yv = __uint_as_float((yb[j >> 1] >> (u * 16)) << 16);
+                                qv[u] = d.fast ? div_rn<true>(d, yv) : div_rn<false>(d, yv);
+                            }
+                            const uint32_t c2 =
+                                __nv_cvt_float2_to_fp8x2(make_float2(qv[0], qv[1]), __NV_SATFINITE, __NV_E4M3);
+                            if (row < mlim) {
+                                const int col = g * 16 + j;
+                                if (col < it.nrows) dst8[(size_t)(it.row0 + col) * a.out_ld] = (uint8_t)c2;
+                                if (col + 1 < it.nrows)
+                                    dst8[(size_t)(it.row0 + col + 1) * a.out_ld] = (uint8_t)(c2 >> 8);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xfree);  // this warp's reads of the maxima are done
+                ++xph;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+                if (++acc == C::kNumAcc) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+                continue;
+            }
             for (int g = part; g < nb; g += kEpiWarps / 4) {
                 float v0[16], v1[16];
                 tmem_ld16(tl + g * 16, v0);
@@ -478,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 tmem_ld_wait();
                 // FP8 down: the token-row scales of this column group
                 float sxv[16];
-                if (MODE == kDownF8) {
+                if (Traits<MODE>::kDownF8Like) {
                     const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -491,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 for (int hh = 0; hh < NA; ++hh) {
                     const int row = mrow + hh * 128;
                     if (row >= mlim) continue;
-                    if (MODE == kDownF8) {
+                    if (Traits<MODE>::kDownF8Like) {
                         // dequantise: weight-row scale x intermediate-row scale
                         const float sw = it.shared ? __ldg(a.sa0_scale + row)
                                                    : __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row);
@@ -570,16 +702,19 @@ cudaError_t launch_gemm(GemmMode mode, int bn, const GemmArgs& args, int grid, c
             case kGateUp: return launch_one<kGateUp, 32, 5>(args, grid, stream);
             case kDown: return launch_one<kDown, 32, 5>(args, grid, stream);
             case kDownF8: return launch_one<kDownF8, 32, 5>(args, grid, stream);
+            case kDownF8Q: return launch_one<kDownF8Q, 32, 5>(args, grid, stream);
             case kRouter: return launch_one<kRouter, 32, 8>(args, grid, stream);
         }
     } else if (bn == kMidBN) {
         if (mode == kDownF8) return launch_one<kDownF8, kMidBN, 4>(args, grid, stream);
+        if (mode == kDownF8Q) return launch_one<kDownF8Q, kMidBN, 4>(args, grid, stream);
     } else if (bn == kPrefillBN) {
         switch (mode) {
             case kGateUpF8: return launch_one<kGateUpF8, kPrefillBN, 4>(args, grid, stream);
             case kGateUp: return launch_one<kGateUp, kPrefillBN, 4>(args, grid, stream);
             case kDown: return launch_one<kDown, kPrefillBN, 4>(args, grid, stream);
             case kDownF8: return launch_one<kDownF8, kPrefillBN, 4>(args, grid, stream);
+            case kDownF8Q: return launch_one<kDownF8Q, kPrefillBN, 4>(args, grid, stream);
             case kRouter: return launch_one<kRouter, kPrefillBN, 5>(args, grid, stream);
         }
     }

@@ -73,7 +73,12 @@ inline cudaError_t configure_once(std::atomic<uint64_t>& done, F&& configure) {
 // (or intermediate) scales applied in the epilogue (they factor out of the K
 // sum).  The FP8 shared down is one matrix [H, n_sh*I_sh] on the concatenated
 // shared intermediate.
-enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2, kGateUpF8 = 3, kDownF8 = 4 };
+// kDownF8Q: kDownF8 whose routed outputs leave as the E4M3 combine payload:
+// each output row's bf16 value quantised in blocks of kPayloadBlock columns
+// (one fp32 scale per block, codes as the row quantiser's); a down item owns
+// 256 consecutive output columns, so every block is reduced inside one CTA.
+enum GemmMode : int { kGateUp = 0, kDown = 1, kRouter = 2, kGateUpF8 = 3, kDownF8 = 4, kDownF8Q = 5 };
+constexpr int kPayloadBlock = MOE_PAYLOAD_BLOCK;
 
 // One launch computes D = A * B^T for a list of work items.  A is a weight
 // tile of 128 output rows (the UMMA M operand), B is a chunk of up to BN
@@ -113,6 +118,10 @@ struct GemmArgs {
     const float* sa1_scale; // shared up rows [n_sh*I_sh]
     const float* b_scale;   // dispatched token rows [T*k] | intermediate rows [T*k]
     const float* sb_scale;  // tokens [T] | shared intermediate rows [T]
+    // kDownF8Q only: the E4M3 combine payload of the routed rows
+    uint8_t* out8;          // codes [T*k, m_routed]
+    float* out8_scale;      // block scales [T*k, n_blk]
+    int n_blk;              // ceil(m_routed / kPayloadBlock)
     DevStatus st;
 };
 
@@ -189,6 +198,10 @@ int dispatch_max_slots();  // slots the index pass's shared-memory histograms ho
 cudaError_t launch_combine(const uint16_t* y_disp, const int32_t* inv_perm, const float* topk_w,
                            const float* y_shared, int T, int k, int hidden, uint16_t* out,
                            cudaStream_t stream);
+
+// E4M3 combine payload: y8 [T*k, hidden] codes, y_scale [T*k, ceil(hidden/kPayloadBlock)].
+cudaError_t launch_combine_fp8(const uint8_t* y8, const float* y_scale, const int32_t* inv_perm, const float* topk_w,
+                               const float* y_shared, int T, int k, int hidden, uint16_t* out, cudaStream_t stream);
 
 int num_sms();
 

@@ -510,10 +510,12 @@ static int down_impl(const moe_shape_t* s, int T, const void* h_disp, const void
     return MOE_OK;
 }
 
+// y8 != null: the routed outputs leave as the E4M3 combine payload (y8 codes,
+// y8_scale block scales) instead of bf16 y_disp.
 static int down_fp8_impl(const moe_shape_t* s, int T, const void* h8, const float* h_scale, const void* hs8,
                          const float* hs_scale, const int32_t* offsets, const void* qd, const float* sd,
                          const void* qsd, const float* ssd, void* y_disp, float* y_shared, int mode,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, uint8_t* y8 = nullptr, float* y8_scale = nullptr) {
     const int n_sh = s->n_shared;
     const int Ks = n_sh * s->inter_shared;  // K of the concatenated shared down matrix
     if (s->inter % 16 || Ks % 16)
@@ -523,7 +525,12 @@ static int down_fp8_impl(const moe_shape_t* s, int T, const void* h8, const floa
     NEED4(offsets, "offsets");
     NEED(qd, "qd");
     NEED4(sd, "sd");
-    NEED(y_disp, "y_disp");
+    if (y8) {
+        NEED(y8, "y_disp8");
+        NEED4(y8_scale, "y_disp_scale");
+    } else {
+        NEED(y_disp, "y_disp");
+    }
     if (n_sh > 0) {
         NEED(hs8, "hs8");
         NEED4(hs_scale, "hs_scale");
@@ -566,8 +573,11 @@ static int down_fp8_impl(const moe_shape_t* s, int T, const void* h8, const floa
     g.sa0_scale = ssd;
     g.b_scale = h_scale;
     g.sb_scale = hs_scale;
+    g.out8 = y8;
+    g.out8_scale = y8_scale;
+    g.n_blk = (s->hidden + kPayloadBlock - 1) / kPayloadBlock;
     g.st = st;
-    MOE_CUDA(launch_gemm(kDownF8, bn, g, num_sms(), stream), "FP8 down gemm launch");
+    MOE_CUDA(launch_gemm(y8 ? kDownF8Q : kDownF8, bn, g, num_sms(), stream), "FP8 down gemm launch");
     return MOE_OK;
 }
 
@@ -581,7 +591,9 @@ struct FwdLayout {
     size_t route, idx, w, slot_of, perm, inv_perm, counts, blocks, offsets, x_disp, ffn, y_disp, y_sh, dispatch, total;
 };
 
-static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
+// with_y_disp = false: no bf16 expert-output buffer (the E4M3 forward carries
+// its own payload buffers instead)
+static FwdLayout fwd_layout(const moe_shape_t* s, int T, bool with_y_disp = true) {
     FwdLayout L;
     const size_t n = (size_t)T * s->top_k;
     size_t off = 0;
@@ -601,7 +613,7 @@ static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
     L.offsets = take((size_t)(s->n_slots + 2) * 4);
     L.x_disp = take(n * s->hidden * 2);
     L.ffn = take(ffn_ws(s, T));
-    L.y_disp = take(n * s->hidden * 2);
+    L.y_disp = take(with_y_disp ? n * s->hidden * 2 : 0);
     L.y_sh = take((size_t)T * s->hidden * 4);
     L.dispatch = take(dispatch_ws(s, T));
     L.total = off;
@@ -612,12 +624,12 @@ static FwdLayout fwd_layout(const moe_shape_t* s, int T) {
 // quantised intermediates (routed rows, shared rows)
 struct FwdLayoutF8 {
     FwdLayout base;
-    size_t x8, x_scale, x_disp8, x_disp_scale, h8, h_scale, hs8, hs_scale, total;
+    size_t x8, x_scale, x_disp8, x_disp_scale, h8, h_scale, hs8, hs_scale, y8, y_scale, total;
 };
 
 static FwdLayoutF8 fwd_layout_f8(const moe_shape_t* s, int T) {
     FwdLayoutF8 L;
-    L.base = fwd_layout(s, T);
+    L.base = fwd_layout(s, T, false);
     const size_t n = (size_t)T * s->top_k;
     size_t off = L.base.total;
     auto take = [&](size_t bytes) {
@@ -633,6 +645,8 @@ static FwdLayoutF8 fwd_layout_f8(const moe_shape_t* s, int T) {
     L.h_scale = take(n * 4);
     L.hs8 = take((size_t)T * s->n_shared * s->inter_shared);
     L.hs_scale = take((size_t)T * 4);
+    L.y8 = take(n * s->hidden);
+    L.y_scale = take(n * (size_t)((s->hidden + kPayloadBlock - 1) / kPayloadBlock) * 4);
     L.total = off;
     return L;
 }
@@ -1023,6 +1037,39 @@ int moe_expert_down_fp8(const moe_shape_t* shape, int T, const uint8_t* h8, cons
                          as_stream(stream));
 }
 
+int moe_expert_down_fp8_payload(const moe_shape_t* shape, int T, const uint8_t* h8, const float* h_scale,
+                                const uint8_t* hs8, const float* hs_scale, const int32_t* offsets, const uint8_t* qd,
+                                const float* sd, const uint8_t* qsd, const float* ssd, uint8_t* y_disp8,
+                                float* y_disp_scale, float* y_shared, int mode, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
+    int rc = check_shape(shape, T);
+    if (rc) return rc;
+    if (mode < MOE_FFN_AUTO || mode > MOE_FFN_PREFILL) return fail(MOE_ERR_INVALID_ARG, "bad mode %d", mode);
+    if (shape->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
+    if (T == 0) return MOE_OK;
+    return down_fp8_impl(shape, T, h8, h_scale, hs8, hs_scale, offsets, qd, sd, qsd, ssd, nullptr, y_shared, mode,
+                         as_stream(stream), y_disp8, y_disp_scale);
+}
+
+int moe_combine_fp8(const moe_shape_t* shape, int T, const uint8_t* y_disp8, const float* y_disp_scale,
+                    const int32_t* inv_perm, const float* topk_w, const float* y_shared, void* out, void* stream) {
+    PdlScope pdl((long)T * (shape ? shape->top_k : 0));
+    int rc = check_shape(shape, T);
+    if (rc) return rc;
+    if (shape->hidden % 16) return fail(MOE_ERR_INVALID_ARG, "FP8 rows need hidden %% 16 == 0");
+    if (T == 0) return MOE_OK;
+    NEED(y_disp8, "y_disp8");
+    NEED4(y_disp_scale, "y_disp_scale");
+    NEED4(inv_perm, "inv_perm");
+    NEED4(topk_w, "topk_w");
+    NEED(out, "out");
+    if (y_shared) NEED(y_shared, "y_shared");
+    MOE_CUDA(launch_combine_fp8(y_disp8, y_disp_scale, inv_perm, topk_w, y_shared, T, shape->top_k, shape->hidden,
+                                static_cast<uint16_t*>(out), as_stream(stream)),
+             "E4M3 combine launch");
+    return MOE_OK;
+}
+
 size_t moe_workspace_size_fp8(const moe_shape_t* shape, int T) {
     if (check_shape(shape, T)) return 0;
     return fwd_layout_f8(shape, T).total;
@@ -1082,10 +1129,13 @@ int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, const void* 
     if (Ks > 0)
         MOE_CUDA(launch_quantize_rows(reinterpret_cast<const uint16_t*>(hs), T, Ks, b + L.hs8, hs_scale, st),
                  "shared intermediate quantize launch");
-    if ((rc = moe_expert_down_fp8(shape, T, b + L.h8, h_scale, Ks > 0 ? b + L.hs8 : nullptr, hs_scale, offsets, qd,
-                                  sd, qsd, ssd, b + B.y_disp, y_sh, mode, stream)))
+    // expert outputs leave as the E4M3 combine payload (codes + one scale per 128-column block)
+    uint8_t* y8 = b + L.y8;
+    float* y_scale = reinterpret_cast<float*>(b + L.y_scale);
+    if ((rc = moe_expert_down_fp8_payload(shape, T, b + L.h8, h_scale, Ks > 0 ? b + L.hs8 : nullptr, hs_scale,
+                                          offsets, qd, sd, qsd, ssd, y8, y_scale, y_sh, mode, stream)))
         return rc;
-    return moe_combine(shape, T, b + B.y_disp, inv, tw, y_sh, out, stream);
+    return moe_combine_fp8(shape, T, y8, y_scale, inv, tw, y_sh, out, stream);
 }
 
 }  // extern "C"

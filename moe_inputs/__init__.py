@@ -254,6 +254,21 @@ def hidden_states(w: Workload, device="cpu", rows: Optional[slice] = None) -> to
     return normal_bf16((r1 - r0, w.hidden), 1.0, w.seed, TID_X, 0, device, offset=r0 * w.hidden)
 
 
+def with_outliers(x: torch.Tensor, seed: int, per_row: int = 2, lo: float = 8.0, hi: float = 20.0) -> torch.Tensor:
+    """A copy of x [T, H] (unit-variance rows) with per_row seeded entries of every
+    row replaced by outliers of magnitude lo..hi (in units of the row's standard
+    deviation, 1) and random sign, rounded to bf16: heavy tails the bounded
+    generator (+-3.45 sigma) never produces."""
+    T, H = x.shape
+    rng = np.random.Generator(np.random.PCG64([seed, 0x0D7]))
+    cols = np.stack([rng.choice(H, size=per_row, replace=False) for _ in range(T)])
+    mag = rng.uniform(lo, hi, size=(T, per_row)) * rng.choice([-1.0, 1.0], size=(T, per_row))
+    out = x.clone()
+    rows = torch.arange(T)[:, None].expand(T, per_row)
+    out[rows, torch.from_numpy(cols)] = torch.from_numpy(mag).to(torch.float32).to(torch.bfloat16).to(x.device)
+    return out
+
+
 def router_weight(w: Workload, device="cpu") -> torch.Tensor:
     """W_r stored [E, H] (row e = expert e's router vector), bf16 ~ N(0, 0.02**2)."""
     return normal_bf16((w.n_experts, w.hidden), w.router_std, w.seed, TID_ROUTER, 0, device)

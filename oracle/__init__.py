@@ -396,15 +396,24 @@ def quantize_layer_fp8(w, w_gate, w_up, w_down, ws_gate, ws_up, ws_down) -> dict
 
 
 def moe_forward_fp8(w, x, w_router, bias, replica_of, q):
-    """Layer in FP8 (payload and every expert matrix); q as quantize_layer_fp8 returns."""
+    """Layer in FP8 (payloads and every expert matrix); q as quantize_layer_fp8 returns.
+
+    Also returns the combine weights [T,k], inv_perm [T*k] and the E4M3 combine
+    payload (y_codes [T*k, H], y_scale [T*k, nb], rows in dispatch order)."""
     T = x.shape[0]
+    n = T * w.top_k
+    nb = (w.hidden + PAYLOAD_BLOCK - 1) // PAYLOAD_BLOCK
     idx = np.empty((T, w.top_k), np.int32)
     out = np.empty((T, w.hidden), np.float64)
+    weight = np.empty((T, w.top_k), np.float64)
+    inv = np.empty(n, np.int32)
+    y_codes = np.empty((n, w.hidden), np.uint8)
+    y_scale = np.empty((n, nb), np.float32)
     a = {k_: (_u8(q[k_]) if k_.startswith("q") else _f32(q[k_]))
          for k_ in ("qg", "sg", "qu", "su", "qd", "sd", "qsg", "ssg", "qsu", "ssu", "qsd", "ssd")}
-    inv = lib().oracle_moe_forward_fp8(
+    invalid = lib().oracle_moe_forward_fp8_payload(
         ctypes.byref(shape_of(w)), T, _ptr(_u16(x)), _ptr(_u16(w_router)), _ptr(_f32(bias)),
         _ptr(_i32(replica_of)), *(_ptr(a[k_]) for k_ in ("qg", "sg", "qu", "su", "qd", "sd", "qsg", "ssg", "qsu",
                                                         "ssu", "qsd", "ssd")),
-        _ptr(idx), _ptr(out))
-    return dict(idx=idx, out=out, invalid=inv)
+        _ptr(idx), _ptr(out), _ptr(weight), _ptr(inv), _ptr(y_codes), _ptr(y_scale))
+    return dict(idx=idx, out=out, invalid=invalid, weight=weight, inv_perm=inv, y_codes=y_codes, y_scale=y_scale)

@@ -585,6 +585,16 @@ int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, cons
                            const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd,
                            const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
                            const uint8_t* qsd, const float* ssd, int32_t* idx, double* out) {
+    return oracle_moe_forward_fp8_payload(s, T, x, w_router, bias, replica_of, qg, sg, qu, su, qd, sd, qsg, ssg, qsu,
+                                          ssu, qsd, ssd, idx, out, NULL, NULL, NULL, NULL);
+}
+
+int oracle_moe_forward_fp8_payload(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
+                                   const float* bias, const int32_t* replica_of, const uint8_t* qg, const float* sg,
+                                   const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd,
+                                   const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
+                                   const uint8_t* qsd, const float* ssd, int32_t* idx, double* out, double* weight,
+                                   int32_t* inv_perm, uint8_t* y_codes, float* y_scale) {
     const int H = s->hidden, E = s->n_experts, k = s->top_k, S = s->n_slots, I = s->inter;
     const size_t n = (size_t)T * k;
     double* logits = (double*)malloc((size_t)T * E * sizeof(double));
@@ -613,10 +623,12 @@ int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, cons
                                   sd + (size_t)slot * H, yd + (size_t)row * H);
         }
     }
-    oracle_payload_e4m3((int)n, H, yd, yd, NULL, NULL);  /* in place: each row read before it is written */
+    oracle_payload_e4m3((int)n, H, yd, yd, y_codes, y_scale);  /* in place: each row read before it is written */
     for (int t = 0; t < T; ++t)
         oracle_shared_row_fp8(s, qx + (size_t)t * H, sx[t], qsg, ssg, qsu, ssu, qsd, ssd, ysh + (size_t)t * H);
     oracle_combine(s, T, yd, inv, w, ysh, out);
+    if (weight) memcpy(weight, w, n * sizeof(double));
+    if (inv_perm) memcpy(inv_perm, inv, n * sizeof(int32_t));
     free(logits); free(w); free(so); free(cnt); free(off); free(perm); free(inv);
     free(qx); free(sx); free(yd); free(ysh);
     return invalid;

@@ -212,6 +212,16 @@ int oracle_moe_forward_fp8(const oracle_shape* s, int T, const uint16_t* x, cons
                            const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
                            const uint8_t* qsd, const float* ssd, int32_t* idx, double* out);
 
+/* oracle_moe_forward_fp8 that also returns the combine weights weight [T*k],
+ * inv_perm [T*k] and the payload (y_codes [T*k, H] and y_scale [T*k,
+ * ceil(H/ORACLE_PAYLOAD_BLOCK)], rows in dispatch order); any may be NULL. */
+int oracle_moe_forward_fp8_payload(const oracle_shape* s, int T, const uint16_t* x, const uint16_t* w_router,
+                                   const float* bias, const int32_t* replica_of, const uint8_t* qg, const float* sg,
+                                   const uint8_t* qu, const float* su, const uint8_t* qd, const float* sd,
+                                   const uint8_t* qsg, const float* ssg, const uint8_t* qsu, const float* ssu,
+                                   const uint8_t* qsd, const float* ssd, int32_t* idx, double* out, double* weight,
+                                   int32_t* inv_perm, uint8_t* y_codes, float* y_scale);
+
 /* Replica placement for n_rep redundant slots from per-expert counts[E].
  * Hot list: the n_rep experts with the largest counts (ties -> lower id).
  * Each block initially carries the load of its experts, a hot expert's

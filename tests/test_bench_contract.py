@@ -44,10 +44,10 @@ def test_algorithmic_bytes_and_flops():
     want = 163 * per_slot + 2 * 3 * H * 2048 * 2 + E * H * 2 + T * H * 2 + 2 * T * k * H * 2 * 2 + T * H * 2
     assert bf["bytes"] == want and bf["touched"] == 163
     assert bf["flops"] == 6 * H * I * T * k + 6 * H * 2048 * 2 * T + 2 * T * H * E
-    # E4M3: every expert weight and the dispatch payload at one byte
+    # E4M3: every expert weight and both payloads at one byte, the combine payload with 56 block scales a row
     bf8 = bench.layer_bytes_flops(w, counts, fp8=True)
-    want8 = 163 * per_slot // 2 + 2 * 3 * H * 2048 + E * H * 2 + T * H * 2 + 2 * T * k * H + 2 * T * k * H * 2 + \
-        T * H * 2
+    want8 = 163 * per_slot // 2 + 2 * 3 * H * 2048 + E * H * 2 + T * H * 2 + 2 * T * k * H + \
+        2 * T * k * (H + 56 * 4) + T * H * 2
     assert bf8["bytes"] == want8
 
 

@@ -122,7 +122,12 @@ def test_pointer_and_workspace_validation_codes():
     assert L.moe_dispatch(*args, mis, need, None) == m.MOE_ERR_INVALID_ARG
     assert L.moe_dispatch_fp8(ctypes.byref(s), 4096, *([b] * 13), None, 0, None) == m.MOE_ERR_WORKSPACE
     fw8 = L.moe_workspace_size_fp8(ctypes.byref(s), 4096)
-    assert fw8 >= L.moe_workspace_size(ctypes.byref(s), 4096) + 4096 * 8 * 7168
+    fw = L.moe_workspace_size(ctypes.byref(s), 4096)
+    n = 4096 * 8
+    # the E4M3 forward holds both E4M3 payloads (dispatch: n*H codes; combine: n*H codes and n*56 block
+    # scales) in place of the bf16 combine payload (n*H*2 bytes)
+    assert fw8 >= fw - n * 7168 * 2 + 2 * n * 7168 + n * 56 * 4
+    assert fw8 < fw + n * 7168
 
 
 def test_empty_batch_is_a_no_op():

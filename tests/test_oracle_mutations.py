@@ -52,7 +52,7 @@ MUTANTS = [
     ("payload scale per row instead of per block",
      "oracle_quantize_blocks_e4m3(1, cols, ORACLE_PAYLOAD_BLOCK, yb, q, sc);",
      "oracle_quantize_blocks_e4m3(1, cols, cols, yb, q, sc);\n        for (int b = 1; b < nb; ++b) sc[b] = sc[0];"),
-    ("payload skipped in the E4M3 layer", "oracle_payload_e4m3((int)n, H, yd, yd, NULL, NULL);", "(void)n;"),
+    ("payload skipped in the E4M3 layer", "oracle_payload_e4m3((int)n, H, yd, yd, y_codes, y_scale);", "(void)n;"),
     ("payload dequantised with the wrong block's scale",
      "oracle_e4m3_decode(q[c]) * (double)sc[c / ORACLE_PAYLOAD_BLOCK];",
      "oracle_e4m3_decode(q[c]) * (double)sc[(c / ORACLE_PAYLOAD_BLOCK + 1) % nb];"),
