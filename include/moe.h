@@ -399,6 +399,40 @@ MOE_API int moe_forward_fp8(const moe_shape_t* shape, int T, const void* x, cons
 MOE_API int moe_combine(const moe_shape_t* shape, int T, const void* y_disp, const int32_t* inv_perm,
                 const float* topk_w, const float* y_shared, void* out, void* stream);
 
+/* ---------------------------------------------------------------- EP across GPUs
+ * Section 2.1: EP rank g holds the slots of block g; section 2.2 steps 2 and 4:
+ * the dispatch all-to-all sends a token's rows to the ranks holding its
+ * experts, the combine all-to-all brings the expert outputs back (section 2.3:
+ * 2 * k * hidden * 2 bytes per token).  The collectives themselves are the
+ * caller's (NCCL, or torch.distributed over it); these calls do the
+ * bookkeeping around them.  world = n_blocks ranks, spb = n_slots / world.
+ *
+ * moe_ep_plan (host only, no device memory):
+ *   counts [n_slots+1]: this rank's dispatch counts (moe_dispatch);
+ *   recv_counts [world*spb]: recv_counts[s*spb+j] = rows source rank s sends
+ *     for local slot j (rank s's counts of this rank's slots, exchanged first);
+ *   out: send_rows [world] (rows to each rank: the segment of its block in the
+ *     dispatch buffer, in rank order), recv_rows [world] (rows from each source,
+ *     received source-major, each source's rows in slot order),
+ *   local_offsets [spb+2]: offsets of the local slots once regrouped
+ *     slot-major (each slot's rows from source 0, 1, ...); [spb] = [spb+1] = R;
+ *   slot_from_src [R] / src_from_slot [R] (either may be NULL): the
+ *     source-major index of each slot-major row, and its inverse; rows_cap is
+ *     their capacity; *rows_out = R, the rows this rank receives.
+ *   Errors: MOE_ERR_INVALID_ARG (world != n_blocks, null, negative counts,
+ *   R > rows_cap when a map is asked for), MOE_ERR_UNSUPPORTED (>= 2^31 rows).
+ * moe_gather_rows: dst[i] = src[index[i]] for n_rows rows of row_bytes bytes
+ *   (row_bytes % 16 == 0, src and dst 16-byte aligned, device pointers;
+ *   index [n_rows] device int32, each in range of src: not checked), async on
+ *   stream.  Regroups received rows slot-major (index = slot_from_src) and
+ *   expert outputs back source-major (index = src_from_slot), for bf16 and
+ *   E4M3 rows alike. */
+MOE_API int moe_ep_plan(const moe_shape_t* shape, int world, const int32_t* counts, const int32_t* recv_counts,
+                        int32_t* send_rows, int32_t* recv_rows, int32_t* local_offsets, int32_t* slot_from_src,
+                        int32_t* src_from_slot, int32_t rows_cap, int32_t* rows_out);
+MOE_API int moe_gather_rows(int n_rows, int row_bytes, const void* src, const int32_t* index, void* dst,
+                            void* stream);
+
 /* ---------------------------------------------------------------- whole layer
  * moe_route (from x), moe_dispatch, moe_expert_ffn, moe_combine on one stream
  * (7 kernel launches; capturable in a CUDA graph).  Intermediates live in the

@@ -39,7 +39,7 @@ EXPORTS = (
     "moe_eplb_window_bytes", "moe_eplb_window_reset", "moe_eplb_window_push", "moe_eplb_stable_table",
     "moe_eplb_copy_replicas", "moe_quantize_rows_fp8", "moe_dispatch_fp8", "moe_expert_gate_up_fp8",
     "moe_workspace_size_fp8", "moe_forward_fp8", "moe_expert_down_fp8", "moe_dispatch_workspace_size",
-    "moe_expert_down_fp8_payload", "moe_combine_fp8",
+    "moe_expert_down_fp8_payload", "moe_combine_fp8", "moe_ep_plan", "moe_gather_rows",
 )
 
 # columns per scale of the E4M3 combine payload (MOE_PAYLOAD_BLOCK in include/moe.h)
@@ -102,6 +102,8 @@ _SIG = {
     "moe_expert_down_fp8": (_I, [_P, _I] + [_P] * 11 + [_I, _P]),
     "moe_expert_down_fp8_payload": (_I, [_P, _I] + [_P] * 12 + [_I, _P]),
     "moe_combine_fp8": (_I, [_P, _I] + [_P] * 7),
+    "moe_ep_plan": (_I, [_P, _I] + [_P] * 7 + [ctypes.c_int32, _P]),
+    "moe_gather_rows": (_I, [_I, _I, _P, _P, _P, _P]),
     "moe_forward_fp8": (_I, [_P, _I] + [_P] * 21 + [_I, _P, _Z, _P]),
     "moe_workspace_size": (_Z, [_P, _I]),
     "moe_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _Z, _P]),
@@ -382,3 +384,39 @@ def moe_forward_fp8(shape, T, x, w_router, bias, replica_of, qg, sg, qu, su, qd,
                                  _ptr(qsu), _ptr(ssu), _ptr(qsd), _ptr(ssd), _ptr(out), _ptr(topk_idx_out),
                                  _ptr(topk_w_out), _ptr(counts_out), _ptr(block_counts_out), mode, _ptr(ws),
                                  ws_bytes, _stream(stream)))
+
+
+# ------------------------------------------------------------------ EP across GPUs (bookkeeping)
+
+def moe_ep_plan(shape, world: int, counts, recv_counts, maps: bool = True):
+    """Host plan of the two all-to-alls of one EP rank (include/moe.h).
+
+    counts: this rank's dispatch counts [n_slots+1]; recv_counts: [world, spb]
+    rows each source sends for each local slot.  Returns a dict of numpy int32
+    arrays: send_rows, recv_rows, local_offsets and (maps) slot_from_src,
+    src_from_slot, plus rows (R)."""
+    import numpy as np
+    spb = shape.n_slots // world
+    c = np.ascontiguousarray(np.asarray(counts).reshape(-1), dtype=np.int32)
+    rc_ = np.ascontiguousarray(np.asarray(recv_counts).reshape(-1), dtype=np.int32)
+    assert c.size == shape.n_slots + 1 and rc_.size == world * spb
+    send, recv = np.empty(world, np.int32), np.empty(world, np.int32)
+    loc = np.empty(spb + 2, np.int32)
+    R = int(rc_.sum())
+    sfs = np.empty(max(1, R), np.int32) if maps else None
+    ssf = np.empty(max(1, R), np.int32) if maps else None
+    rows = ctypes.c_int32()
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+    _check(lib().moe_ep_plan(_shape(shape), world, p(c), p(rc_), p(send), p(recv), p(loc), p(sfs), p(ssf),
+                             max(1, R), ctypes.byref(rows)))
+    out = dict(send_rows=send, recv_rows=recv, local_offsets=loc, rows=rows.value)
+    if maps:
+        out["slot_from_src"], out["src_from_slot"] = sfs[:R], ssf[:R]
+    return out
+
+
+def moe_gather_rows(src, index, dst, stream=None):
+    """dst[i] = src[index[i]] for rows of src (device tensors, rows of a multiple of 16 bytes)."""
+    n = index.numel()
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else dst[0].numel() * dst.element_size()
+    _check(lib().moe_gather_rows(n, row_bytes, _ptr(src), _ptr(index), _ptr(dst), _stream(stream)))

@@ -44,7 +44,8 @@ def test_binding_signatures_match_the_header():
     src = open(HEADER).read()
     decls = re.findall(r"^MOE_API [^(]*?\b(moe_\w+)\(([^;]*?)\);", src, flags=re.M | re.S)
     assert len(decls) == len(m.EXPORTS)
-    kinds = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "double": ctypes.c_double, "uint64_t": ctypes.c_uint64}
+    kinds = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "double": ctypes.c_double, "uint64_t": ctypes.c_uint64,
+             "int32_t": ctypes.c_int32}
     for name, params in decls:
         params = " ".join(params.split())
         plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
