@@ -502,43 +502,49 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 float* xw = xchg + (size_t)(part * 4 + q) * kMaxG * 2 * 16;
                 const float* xp = xchg + (size_t)part * 4 * kMaxG * 2 * 16;
                 const uint32_t xfull = smem_u32(&xbar[part]), xfree = smem_u32(&xbar[4 + part]);
-                // bf16 value of accumulator column group g, half hh of this lane's row
-                auto load_y = [&](int g, int hh, uint32_t (&yb)[8]) {
-                    float v[16];
+                // weight-row scales of this lane's two rows (rows past H are 0), loaded once
+                const float sw[2] = {mrow < mlim ? __ldg(swp + mrow) : 0.0f,
+                                     mrow + 128 < mlim ? __ldg(swp + mrow + 128) : 0.0f};
+                // the 16 token scales of column group g (0 past the chunk's rows), for both halves
+                auto load_sx = [&](int g, float (&sx)[16]) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = g * 16 + j;
+                        sx[j] = col < it.nrows ? __ldg(sbp + col) : 0.0f;
+                    }
+                };
+                // y of group g, half hh: the fp32 value the plain E4M3 down rounds to bf16
+                auto load_y = [&](int g, int hh, const float (&sx)[16], float (&v)[16]) {
                     tmem_ld16(tl + hh * BN + g * 16, v);
                     tmem_ld_wait();
-                    const int row = mrow + hh * 128;
-                    const float sw = row < mlim ? __ldg(swp + row) : 0.0f;  // rows past H are 0
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const int col = g * 16 + j;
-                        const float s0 = col < it.nrows ? __ldg(sbp + col) : 0.0f;
-                        const float s1 = col + 1 < it.nrows ? __ldg(sbp + col + 1) : 0.0f;
-                        const __nv_bfloat162 p2 = __floats2bfloat162_rn(v[j] * (sw * s0), v[j + 1] * (sw * s1));
-                        yb[j >> 1] = *reinterpret_cast<const uint32_t*>(&p2);
-                    }
+                    for (int j = 0; j < 16; ++j) v[j] *= sw[hh] * sx[j];
                 };
                 // the four warps have read the previous item's maxima
                 if (xph > 0 && !mbar_wait(xfree, (xph - 1) & 1, limit)) {
                     ok = false;
                     break;
                 }
+                // pass 1: per column the largest |y| of this warp's 32 rows, rounded to bf16
+                // (rounding is monotone: the bf16 of the largest |y| is the largest bf16 |y|)
 #pragma unroll 1
                 for (int gi = 0; gi < kMaxG; ++gi) {
                     const int g = part + gi * (kEpiWarps / 4);
                     if (g >= nb) break;
+                    float sx[16];
+                    load_sx(g, sx);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         if (it.m0 + hh * 128 >= mlim) break;  // a half past the last output row: no block
-                        uint32_t yb[8];
-                        load_y(g, hh, yb);
+                        float v[16];
+                        load_y(g, hh, sx, v);
                         float mine = 0.0f;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const uint32_t mx = __reduce_max_sync(0xffffffffu, (yb[j >> 1] >> ((j & 1) * 16)) & 0x7fffu);
-                            if (lane == j) mine = __uint_as_float(mx << 16);
+                            const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
+                            if (lane == j) mine = __uint_as_float(mx);
                         }
-                        if (lane < 16) xw[(gi * 2 + hh) * 16 + lane] = mine;
+                        if (lane < 16) xw[(gi * 2 + hh) * 16 + lane] = __bfloat162float(__float2bfloat16_rn(mine));
                     }
                 }
                 __syncwarp();
@@ -547,10 +553,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     ok = false;
                     break;
                 }
+                // pass 2: block scales, codes of the bf16 values, stores
 #pragma unroll 1
                 for (int gi = 0; gi < kMaxG; ++gi) {
                     const int g = part + gi * (kEpiWarps / 4);
                     if (g >= nb) break;
+                    float sx[16];
+                    load_sx(g, sx);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         if (it.m0 + hh * 128 >= mlim) break;
@@ -565,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         if (q == 0 && lane < 16 && col_l < it.nrows)
                             a.out8_scale[(size_t)(it.row0 + col_l) * a.n_blk + blk] = sl;
                         const RowDiv dl = row_div(sl);
-                        uint32_t yb[8];
-                        load_y(g, hh, yb);
+                        float v[16];
+                        load_y(g, hh, sx, v);
                         uint8_t* dst8 = a.out8 + row;
 #pragma unroll
                         for (int j = 0; j < 16; j += 2) {
@@ -577,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                                 d.s = __shfl_sync(0xffffffffu, dl.s, j + u);
                                 d.r = __shfl_sync(0xffffffffu, dl.r, j + u);
                                 d.fast = d.s >= 0x1p-96f;
-                                const float yv = __uint_as_float((yb[j >> 1] >> (u * 16)) << 16);
+                                const float yv = __bfloat162float(__float2bfloat16_rn(v[j + u]));
                                 qv[u] = d.fast ? div_rn<true>(d, yv) : div_rn<false>(d, yv);
                             }
                             const uint32_t c2 =
