@@ -4,7 +4,7 @@ Default workload: the DeepSeek-V3 MoE layer decode step (T=32 tokens, hidden
 7168, 256 routed experts SwiGLU 2048, top-8, 2 shared experts, bf16,
 near-uniform routing), every input resident in HBM.  One step = one forward
 pass of the layer over the batch: router GEMM + top-k, dispatch, expert
-gate/up, expert down, combine (6 kernels of libmoe).
+gate/up, expert down, combine (7 kernels of libmoe).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
@@ -335,12 +335,10 @@ def measure(m, args, w, dev, rank, world, local_rank, weights, with_cpu_baseline
         else:
             m.moe_combine(w, T, y, inv, tw, ysh, out)
 
-    # router (one kernel up to 256 experts; GEMM + top-k above, or with group-limited routing), index
-    # pass (three launches in chunks for large batches), scatter (E4M3: + token quantisation), gate/up,
-    # (E4M3: + intermediate quantisation), down, combine
+    # router GEMM + top-k, index pass (three launches in chunks for large batches), scatter
+    # (E4M3: + token quantisation), gate/up, (E4M3: + intermediate quantisation), down, combine
     index_launches = 3 if m.moe_dispatch_workspace_size(w, T) > 0 else 1
-    route_launches = 1 if (E <= 256 and k <= 32 and not groups) else 2
-    launches_per_step = route_launches + index_launches + 1 + 1 + 1 + 1
+    launches_per_step = 2 + index_launches + 1 + 1 + 1 + 1
     if fp8:
         launches_per_step += 1 + 1 + (w.n_shared > 0)
     for _ in range(args.warmup):

@@ -136,18 +136,11 @@ MOE_API int moe_debug_expire_wait(void* stream);
  * NULL.  logits_in [T,E] fp32 or NULL: when given, the GEMM is skipped and the
  * selection runs on these final logits (bias must then be NULL; x, w_router
  * may be NULL).  logits_out [T,E] fp32 or NULL receives the logits used.
- * With at most 256 experts and k <= 32 the whole step is one kernel: a
- * thread-block cluster per chunk of tokens (16 CTAs a chunk of 32 tokens for
- * batches of up to 32; 8 CTAs a chunk of 128 above) splits K that many ways,
- * and the partial logits are summed across the cluster in rank order before
- * the softmax and the selection.  Otherwise (more experts, or the cluster does not fit) the
- * GEMM writes its K-split partials to ws and a second kernel sums them in a
- * fixed order, the number of splits following T and the device's SM count.
- * Either way results repeat bit for bit on one GPU model and may differ in the
- * last bits of the logits on another.
+ * The GEMM sums K in splits whose number follows T and the device's SM
+ * count, added in a fixed order: results repeat bit for bit on one GPU model
+ * and may differ in the last bits of the logits on another.
  * Outputs topk_idx [T,k] int32, topk_w [T,k] fp32.  ws: device workspace of
- * at least moe_route_workspace_size() bytes (may be NULL if that is 0; the
- * one-kernel path does not touch it). */
+ * at least moe_route_workspace_size() bytes (may be NULL if that is 0). */
 MOE_API size_t moe_route_workspace_size(const moe_shape_t* shape, int T);
 MOE_API int moe_route(const moe_shape_t* shape, int T, const void* x, const void* w_router, const float* bias,
               const float* logits_in, float* logits_out, int32_t* topk_idx, float* topk_w, void* ws,

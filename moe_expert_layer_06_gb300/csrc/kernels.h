@@ -170,17 +170,6 @@ cudaError_t launch_topk(const float* partials, int ksplit, const float* bias, in
                         float* logits_out, int32_t* topk_idx, float* topk_w, int n_groups, int topk_groups,
                         const DevStatus& st, cudaStream_t stream);
 
-// The router in one launch (csrc/router.cu): GEMM, bias, softmax and top-k for
-// at most 256 experts and top-32, one thread-block cluster per token chunk
-// reducing its K split in distributed shared memory.  w: W_r map {H, E, 1} box
-// {64, 128, 1}; x: map {H, 1, T} with box {64, 1, router_fused_bn(T)}.
-// *launched = false (and cudaSuccess) when no cluster can be resident.
-int router_fused_supported(int n_experts, int top_k);
-int router_fused_bn(int T);
-cudaError_t launch_router_fused(const CUtensorMap& w, const CUtensorMap& x, const float* bias, int T, int E, int H,
-                                int k, float* logits_out, int32_t* topk_idx, float* topk_w, const DevStatus& st,
-                                cudaStream_t stream, bool* launched);
-
 // ---------------------------------------------------------------- dispatch / histogram
 struct DispatchArgs {
     int T, k, E, S, n_blocks, hidden;

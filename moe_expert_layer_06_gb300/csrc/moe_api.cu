@@ -274,20 +274,11 @@ static int route_impl(const moe_shape_t* s, int T, int n_groups, int topk_groups
                  "topk launch");
         return MOE_OK;
     }
+    const RoutePlan p = route_plan(s, T);
     GemmArgs g;
     memset(&g, 0, sizeof g);
     if ((rc = tmap_weights(&g.a0, w_router, 1, s->n_experts, s->hidden))) return rc;
     if ((rc = tmap_rows(g.b, x, T, s->hidden))) return rc;
-    if (n_groups == 0 && router_fused_supported(s->n_experts, s->top_k)) {
-        // one launch: the boxes of 32 and 128 token rows are maps 1 and 3
-        bool launched = false;
-        const int j = router_fused_bn(T) == 32 ? 1 : 3;
-        MOE_CUDA(launch_router_fused(g.a0, g.b[j], bias, T, s->n_experts, s->hidden, s->top_k, logits_out, topk_idx,
-                                     topk_w, st, stream, &launched),
-                 "fused router launch");
-        if (launched) return MOE_OK;
-    }
-    const RoutePlan p = route_plan(s, T);
     g.a1 = g.a0;
     g.sa0 = g.sa1 = g.a0;
     for (int j = 0; j < 4; ++j) g.sb[j] = g.b[j];
