@@ -28,6 +28,8 @@
 // drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "e4m3.cuh"
 #include "kernels.h"
 
@@ -78,8 +80,16 @@ struct Config {
     static constexpr int kBBytes = BN * 64 * 2;
     static constexpr int kStageBytes = NA * kABytes + kBBytes;
     static constexpr int kAccCols = NA * BN;
-    static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;
-    static constexpr int kTmemCols = pow2_at_least(kNumAcc * kAccCols);
+    // E4M3 down items whose two tiles' accumulators cannot be double-buffered rotate
+    // three one-tile slots instead: tile u = 2 * (item ordinal) + half goes to slot
+    // u % 3, so the next item's first tile starts at once and its second tile waits
+    // only for the first half of the previous item's epilogue.  An E4M3 down item is
+    // 16 K chunks, so its epilogue is a large share of it (4096 tokens, 160-row
+    // chunks: 957 against 1010 us); the bf16 down item is twice as long and was
+    // slower with the rotation (1446 against 1392 us), so it keeps one accumulator.
+    static constexpr bool kRot = Traits<MODE>::kDownF8Like && 2 * kAccCols > 512 && 3 * BN <= 512;
+    static constexpr int kNumAcc = kRot ? 3 : (2 * kAccCols <= 512) ? 2 : 1;
+    static constexpr int kTmemCols = pow2_at_least(kRot ? 3 * BN : kNumAcc * kAccCols);
     static constexpr int kBarBytes = (2 * STAGES + 2 * kNumAcc + 1) * 8;
     static constexpr int kTableBytes = (kMaxSlots + 4) * 4;
     // column groups of 16 tokens one epilogue warp drains per item
@@ -344,6 +354,74 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 const int nb = (it.nrows + 15) >> 4;
                 const uint32_t idesc =
                     Traits<MODE>::kF8 ? umma_idesc_e4m3(128, nb * 16) : umma_idesc_bf16(128, nb * 16);
+                if (C::kRot) {
+                    // one tile's four MMAs of the chunk in stage st (32 bytes of K each)
+                    auto issue = [&](uint32_t d, int st, int tile, bool first) {
+                        const uint32_t sa = smem_u32(smem + st * C::kStageBytes);
+                        const uint64_t adesc = umma_desc_sw128(sa + tile * kABytes);
+                        const uint64_t bdesc = umma_desc_sw128(sa + NA * kABytes);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
+                            if (Traits<MODE>::kF8) umma_e4m3(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                            else umma_bf16(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, accum);
+                        }
+                    };
+                    // slots of the two tiles and the parities of their current use
+                    const int s0 = acc, s1 = acc == 2 ? 0 : acc + 1;
+                    const uint32_t p0 = acc_phase, p1 = acc == 2 ? acc_phase ^ 1 : acc_phase;
+                    acc += 2;
+                    if (acc >= 3) {
+                        acc -= 3;
+                        acc_phase ^= 1;
+                    }
+                    if (*abort_flag || !mbar_wait(smem_u32(&tempty[s0]), p0 ^ 1, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // The first tile runs ahead over the stages in flight; a stage is released
+                    // once the second tile has consumed it too, so the second tile's MMAs follow
+                    // as soon as its slot is drained.
+                    const int nk = it.kc1 - it.kc0;
+                    int st1 = stage;
+                    int k0 = 0, k1 = 0;
+                    bool t1 = false;
+                    while (k1 < nk) {
+                        if (!t1 && mbar_test_wait(smem_u32(&tempty[s1]), p1 ^ 1)) {
+                            tc_fence_after();
+                            t1 = true;
+                        }
+                        if (t1 && k1 < k0) {
+                            issue(tbase + s1 * BN, st1, 1, k1 == 0);
+                            umma_commit(smem_u32(&empty[st1]));
+                            if (++st1 == STAGES) st1 = 0;
+                            ++k1;
+                        } else if (k0 < nk && k0 - k1 < STAGES) {
+                            if (*abort_flag || !mbar_wait(smem_u32(&full[stage]), phase, limit)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue(tbase + s0 * BN, stage, 0, k0 == 0);
+                            if (++stage == STAGES) {
+                                stage = 0;
+                                phase ^= 1;
+                            }
+                            if (++k0 == nk) umma_commit(smem_u32(&tfull[s0]));
+                        } else {
+                            if (*abort_flag || !mbar_wait(smem_u32(&tempty[s1]), p1 ^ 1, limit)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            t1 = true;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&tfull[s1]));
+                    continue;
+                }
                 if (*abort_flag || !mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1, limit)) {
                     ok = false;
                     break;
@@ -402,9 +480,201 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         uint32_t acc_phase = 0;
         uint32_t xph = 0;  // kDownF8Q: exchanges done by this warp
         bool ok = true;
+        // Rotating slots (kRot): drain one half of a down item (one 128-row output
+        // block) from the TMEM slot at tl.  Routed rows leave as bf16 y (E4M3 operands
+        // dequantised first), shared rows as fp32 y_shared.
+        auto plain_half = [&](const Item& it, int hh, uint32_t tl, int nb, int mlim) {
+            const int row = it.m0 + hh * 128 + q * 32 + lane;
+            const bool live = row < mlim;
+            float sw = 0.0f;
+            if (Traits<MODE>::kDownF8Like && live)
+                sw = it.shared ? __ldg(a.sa0_scale + row) : __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row);
+#pragma unroll 1
+            for (int g = part; g < nb; g += kEpiWarps / 4) {
+                float v[16];
+                tmem_ld16(tl + g * 16, v);
+                tmem_ld_wait();
+                if (!live) continue;
+                if (Traits<MODE>::kDownF8Like) {
+                    const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = g * 16 + j;
+                        v[j] *= sw * (col < it.nrows ? __ldg(sbp + col) : 0.0f);
+                    }
+                }
+                if (it.shared) {
+                    float* dst = reinterpret_cast<float*>(a.out_sh) + row;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = g * 16 + j;
+                        if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_sh_ld] = v[j];
+                    }
+                } else {
+                    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.out) + row;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = g * 16 + j;
+                        if (col < it.nrows) dst[(size_t)(it.row0 + col) * a.out_ld] = __float2bfloat16_rn(v[j]);
+                    }
+                }
+            }
+        };
+        // Rotating slots, E4M3 combine payload: one half is one block of 128 output rows,
+        // so its scales need only this half's maxima.  Pass 1: bf16 y, warp maxima of |y|
+        // per column into shared memory; the four warps of these columns meet; pass 2:
+        // the block scale of each column, codes, stores.
+        // sxg[gi]: lane l's token scale of column group gi (column g*16 + l%16), sw: the
+        // weight-row scale of this lane's row; both loaded before the accumulator wait.
+        auto payload_half = [&](const Item& it, int hh, uint32_t tl, int nb, int mlim,
+                                const float (&sxg)[C::kMaxG], float sw) -> bool {
+            constexpr int kMaxG = C::kMaxG;
+            const int row = it.m0 + hh * 128 + q * 32 + lane;
+            const int blk = (it.m0 >> 7) + hh;
+            float* xw = xchg + (size_t)(part * 4 + q) * kMaxG * 2 * 16;
+            const float* xp = xchg + (size_t)part * 4 * kMaxG * 2 * 16;
+            const uint32_t xfull = smem_u32(&xbar[part]), xfree = smem_u32(&xbar[4 + part]);
+            // y of column group g: the fp32 value the plain E4M3 down rounds to bf16
+            auto load_y = [&](int g, float sxl, float (&v)[16]) {
+                tmem_ld16(tl + g * 16, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] *= sw * __shfl_sync(0xffffffffu, sxl, j);
+            };
+            // the four warps have read the previous exchange's maxima
+            if (xph > 0 && !mbar_wait(xfree, (xph - 1) & 1, limit)) return false;
+#pragma unroll 1
+            for (int gi = 0; gi < kMaxG; ++gi) {
+                const int g = part + gi * (kEpiWarps / 4);
+                if (g >= nb) break;
+                float v[16];
+                load_y(g, sxg[gi], v);
+                // rounding is monotone: the bf16 of the largest |y| is the largest bf16 |y|
+                float mine = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
+                    if (lane == j) mine = __uint_as_float(mx);
+                }
+                if (lane < 16) xw[(gi * 2 + hh) * 16 + lane] = __bfloat162float(__float2bfloat16_rn(mine));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xfull);
+            if (!mbar_wait(xfull, xph & 1, limit)) return false;
+#pragma unroll 1
+            for (int gi = 0; gi < kMaxG; ++gi) {
+                const int g = part + gi * (kEpiWarps / 4);
+                if (g >= nb) break;
+                // lane l < 16: scale of column l from the four warps' maxima
+                const int o = (gi * 2 + hh) * 16 + (lane & 15);
+                const float amax = fmaxf(fmaxf(xp[o], xp[kMaxG * 32 + o]),
+                                         fmaxf(xp[2 * kMaxG * 32 + o], xp[3 * kMaxG * 32 + o]));
+                const float sl = row_scale(amax);
+                const int col_l = g * 16 + lane;
+                if (q == 0 && lane < 16 && col_l < it.nrows)
+                    a.out8_scale[(size_t)(it.row0 + col_l) * a.n_blk + blk] = sl;
+                const RowDiv dl = row_div(sl);
+                float v[16];
+                load_y(g, sxg[gi], v);
+                // codes of the 16 columns, four to a word (byte c of word b: column 4b + c)
+                uint32_t w[4];
+                auto encode = [&](auto all_fast) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        float qv[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            RowDiv d;
+                            d.s = __shfl_sync(0xffffffffu, dl.s, j + u);
+                            d.r = __shfl_sync(0xffffffffu, dl.r, j + u);
+                            const float yv = __bfloat162float(__float2bfloat16_rn(v[j + u]));
+                            if (decltype(all_fast)::value) qv[u] = div_rn<true>(d, yv);
+                            else qv[u] = d.s >= 0x1p-96f ? div_rn<true>(d, yv) : div_rn<false>(d, yv);
+                        }
+                        const uint32_t c2 =
+                            __nv_cvt_float2_to_fp8x2(make_float2(qv[0], qv[1]), __NV_SATFINITE, __NV_E4M3) & 0xffffu;
+                        if (j & 2) w[j >> 2] |= c2 << 16;
+                        else w[j >> 2] = c2;
+                    }
+                };
+                // the reciprocal path for every column unless a scale of this group is
+                // below 2^-96 (lanes 16-31 repeat columns 0-15)
+                if (__all_sync(0xffffffffu, dl.fast)) encode(std::true_type{});
+                else encode(std::false_type{});
+                // 4x4 byte transpose inside each quad of lanes: lane 4m+c ends with column
+                // 4b+c of rows 4m..4m+3, one aligned word (H % 8 == 0, codes 16-byte aligned)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const uint32_t o2 = __shfl_xor_sync(0xffffffffu, w[b], 2);
+                    w[b] = __byte_perm(w[b], o2, (lane & 2) ? 0x3276 : 0x5410);
+                    const uint32_t o1 = __shfl_xor_sync(0xffffffffu, w[b], 1);
+                    w[b] = __byte_perm(w[b], o1, (lane & 1) ? 0x3715 : 0x6240);
+                }
+                const int row4 = it.m0 + hh * 128 + q * 32 + (lane & ~3);
+                if (row4 < mlim) {
+                    uint8_t* dst8 = a.out8 + row4;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int col = g * 16 + 4 * b + (lane & 3);
+                        if (col < it.nrows)
+                            *reinterpret_cast<uint32_t*>(dst8 + (size_t)(it.row0 + col) * a.out_ld) = w[b];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xfree);  // this warp's reads of the maxima are done
+            ++xph;
+            return true;
+        };
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
             const int nb = (it.nrows + 15) >> 4;
+            if (C::kRot) {
+                // the two halves in turn, each from its own slot, each slot freed when drained
+                const int sA = acc, sB = acc == 2 ? 0 : acc + 1;
+                const uint32_t pA = acc_phase, pB = acc == 2 ? acc_phase ^ 1 : acc_phase;
+                acc += 2;
+                if (acc >= 3) {
+                    acc -= 3;
+                    acc_phase ^= 1;
+                }
+                const int mlim = it.shared ? a.m_shared : a.m_routed;
+                // E4M3 payload: the token scales of this warp's column groups and the
+                // weight-row scales of both halves, loaded while the MMAs run
+                float sxg[C::kMaxG], swh[2] = {0.0f, 0.0f};
+                if (MODE == kDownF8Q && !it.shared) {
+#pragma unroll
+                    for (int gi = 0; gi < C::kMaxG; ++gi) {
+                        const int col = (part + gi * (kEpiWarps / 4)) * 16 + (lane & 15);
+                        sxg[gi] = col < it.nrows ? __ldg(a.b_scale + it.row0 + col) : 0.0f;
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int row = it.m0 + hh * 128 + q * 32 + lane;
+                        if (row < mlim) swh[hh] = __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row);
+                    }
+                }
+#pragma unroll 1
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    const int sl = hh ? sB : sA;
+                    if (*abort_flag || !mbar_wait(smem_u32(&tfull[sl]), hh ? pB : pA, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // a half past the last output row (H not a multiple of 256) holds no block
+                    if (it.m0 + hh * 128 < mlim) {
+                        const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + sl * BN;
+                        if (MODE == kDownF8Q && !it.shared) ok = payload_half(it, hh, tl, nb, mlim, sxg, hh ? swh[1] : swh[0]);
+                        else plain_half(it, hh, tl, nb, mlim);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&tempty[sl]));
+                }
+                if (!ok) break;
+                continue;
+            }
             if (*abort_flag || !mbar_wait(smem_u32(&tfull[acc]), acc_phase, limit)) {
                 ok = false;
                 break;
