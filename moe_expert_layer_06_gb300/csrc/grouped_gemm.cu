@@ -529,7 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         auto payload_half = [&](const Item& it, int hh, uint32_t tl, int nb, int mlim,
                                 const float (&sxg)[C::kMaxG], float sw) -> bool {
             constexpr int kMaxG = C::kMaxG;
-            const int row = it.m0 + hh * 128 + q * 32 + lane;
             const int blk = (it.m0 >> 7) + hh;
             float* xw = xchg + (size_t)(part * 4 + q) * kMaxG * 2 * 16;
             const float* xp = xchg + (size_t)part * 4 * kMaxG * 2 * 16;
@@ -626,6 +625,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             ++xph;
             return true;
         };
+        // E4M3 payload: lane l's token scale of each of this warp's column groups
+        // (column g*16 + l%16) and the weight-row scales of its rows in both halves
+        auto payload_scales = [&](const Item& it, int mlim, float (&sxg)[C::kMaxG], float (&swh)[2]) {
+#pragma unroll
+            for (int gi = 0; gi < C::kMaxG; ++gi) {
+                const int col = (part + gi * (kEpiWarps / 4)) * 16 + (lane & 15);
+                sxg[gi] = col < it.nrows ? __ldg(a.b_scale + it.row0 + col) : 0.0f;
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = it.m0 + hh * 128 + q * 32 + lane;
+                swh[hh] = row < mlim ? __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row) : 0.0f;
+            }
+        };
         for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
             const Item it = decode_item<MODE, BN>(i, a, tb, n_sh_items);
             const int nb = (it.nrows + 15) >> 4;
@@ -639,21 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     acc_phase ^= 1;
                 }
                 const int mlim = it.shared ? a.m_shared : a.m_routed;
-                // E4M3 payload: the token scales of this warp's column groups and the
-                // weight-row scales of both halves, loaded while the MMAs run
-                float sxg[C::kMaxG], swh[2] = {0.0f, 0.0f};
-                if (MODE == kDownF8Q && !it.shared) {
-#pragma unroll
-                    for (int gi = 0; gi < C::kMaxG; ++gi) {
-                        const int col = (part + gi * (kEpiWarps / 4)) * 16 + (lane & 15);
-                        sxg[gi] = col < it.nrows ? __ldg(a.b_scale + it.row0 + col) : 0.0f;
-                    }
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int row = it.m0 + hh * 128 + q * 32 + lane;
-                        if (row < mlim) swh[hh] = __ldg(a.a0_scale + (size_t)it.z * a.m_routed + row);
-                    }
-                }
+                // E4M3 payload: the token and weight-row scales, loaded while the MMAs run
+                float sxg[C::kMaxG], swh[2];
+                if (MODE == kDownF8Q && !it.shared) payload_scales(it, mlim, sxg, swh);
 #pragma unroll 1
                 for (int hh = 0; hh < 2 && ok; ++hh) {
                     const int sl = hh ? sB : sA;
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     // a half past the last output row (H not a multiple of 256) holds no block
                     if (it.m0 + hh * 128 < mlim) {
                         const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + sl * BN;
-                        if (MODE == kDownF8Q && !it.shared) ok = payload_half(it, hh, tl, nb, mlim, sxg, hh ? swh[1] : swh[0]);
+                        if (MODE == kDownF8Q && !it.shared) ok = payload_half(it, hh, tl, nb, mlim, sxg, swh[hh]);
                         else plain_half(it, hh, tl, nb, mlim);
                     }
                     tc_fence_before();
@@ -675,13 +676,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 if (!ok) break;
                 continue;
             }
+            const int mlim = it.shared ? a.m_shared : a.m_routed;
+            float sxg[C::kMaxG], swh[2];
+            if (MODE == kDownF8Q && !it.shared) payload_scales(it, mlim, sxg, swh);
             if (*abort_flag || !mbar_wait(smem_u32(&tfull[acc]), acc_phase, limit)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int mrow = it.m0 + q * 32 + lane;
-            const int mlim = it.shared ? a.m_shared : a.m_routed;
             const bool row_ok = mrow < mlim;
             (void)row_ok;
             const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16) + acc * C::kAccCols;
@@ -758,121 +761,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 continue;
             }
             if (MODE == kDownF8Q && !it.shared) {
-                // Routed rows leave as the E4M3 payload: block = 128 output rows (one TMEM
-                // half), one scale per (token, block).  The four warps that drain these
-                // columns hold 32 rows of every block each.  Pass 1: bf16 y, warp maxima
-                // of |y| per column into shared memory; pass 2 (after all four have
-                // written): reload, the block scale of each column, codes, stores.  The
-                // accumulator is held through both passes: the item's outputs do not fit
-                // the 96 registers a thread has at 18 warps (with 10 warps and 168
-                // registers the epilogue took longer than the items it overlapped).
-                constexpr int kMaxG = C::kMaxG;
-                const float* sbp = a.b_scale + it.row0;
-                const float* swp = a.a0_scale + (size_t)it.z * a.m_routed;
-                float* xw = xchg + (size_t)(part * 4 + q) * kMaxG * 2 * 16;
-                const float* xp = xchg + (size_t)part * 4 * kMaxG * 2 * 16;
-                const uint32_t xfull = smem_u32(&xbar[part]), xfree = smem_u32(&xbar[4 + part]);
-                // weight-row scales of this lane's two rows (rows past H are 0), loaded once
-                const float sw[2] = {mrow < mlim ? __ldg(swp + mrow) : 0.0f,
-                                     mrow + 128 < mlim ? __ldg(swp + mrow + 128) : 0.0f};
-                // the 16 token scales of column group g (0 past the chunk's rows), for both halves
-                auto load_sx = [&](int g, float (&sx)[16]) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int col = g * 16 + j;
-                        sx[j] = col < it.nrows ? __ldg(sbp + col) : 0.0f;
-                    }
-                };
-                // y of group g, half hh: the fp32 value the plain E4M3 down rounds to bf16
-                auto load_y = [&](int g, int hh, const float (&sx)[16], float (&v)[16]) {
-                    tmem_ld16(tl + hh * BN + g * 16, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] *= sw[hh] * sx[j];
-                };
-                // the four warps have read the previous item's maxima
-                if (xph > 0 && !mbar_wait(xfree, (xph - 1) & 1, limit)) {
-                    ok = false;
-                    break;
-                }
-                // pass 1: per column the largest |y| of this warp's 32 rows, rounded to bf16
-                // (rounding is monotone: the bf16 of the largest |y| is the largest bf16 |y|)
+                // E4M3 payload, both halves from this accumulator, which is freed after both
 #pragma unroll 1
-                for (int gi = 0; gi < kMaxG; ++gi) {
-                    const int g = part + gi * (kEpiWarps / 4);
-                    if (g >= nb) break;
-                    float sx[16];
-                    load_sx(g, sx);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (it.m0 + hh * 128 >= mlim) break;  // a half past the last output row: no block
-                        float v[16];
-                        load_y(g, hh, sx, v);
-                        float mine = 0.0f;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
-                            if (lane == j) mine = __uint_as_float(mx);
-                        }
-                        if (lane < 16) xw[(gi * 2 + hh) * 16 + lane] = __bfloat162float(__float2bfloat16_rn(mine));
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xfull);
-                if (!mbar_wait(xfull, xph & 1, limit)) {
-                    ok = false;
-                    break;
-                }
-                // pass 2: block scales, codes of the bf16 values, stores
-#pragma unroll 1
-                for (int gi = 0; gi < kMaxG; ++gi) {
-                    const int g = part + gi * (kEpiWarps / 4);
-                    if (g >= nb) break;
-                    float sx[16];
-                    load_sx(g, sx);
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (it.m0 + hh * 128 >= mlim) break;
-                        const int row = mrow + hh * 128;
-                        const int blk = (it.m0 >> 7) + hh;
-                        // lane l < 16: scale of column l's block from the four warps' maxima
-                        const int o = (gi * 2 + hh) * 16 + (lane & 15);
-                        const float amax = fmaxf(fmaxf(xp[o], xp[kMaxG * 32 + o]),
-                                                 fmaxf(xp[2 * kMaxG * 32 + o], xp[3 * kMaxG * 32 + o]));
-                        const float sl = row_scale(amax);
-                        const int col_l = g * 16 + lane;
-                        if (q == 0 && lane < 16 && col_l < it.nrows)
-                            a.out8_scale[(size_t)(it.row0 + col_l) * a.n_blk + blk] = sl;
-                        const RowDiv dl = row_div(sl);
-                        float v[16];
-                        load_y(g, hh, sx, v);
-                        uint8_t* dst8 = a.out8 + row;
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            float qv[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                RowDiv d;
-                                d.s = __shfl_sync(0xffffffffu, dl.s, j + u);
-                                d.r = __shfl_sync(0xffffffffu, dl.r, j + u);
-                                d.fast = d.s >= 0x1p-96f;
-                                const float yv = __bfloat162float(__float2bfloat16_rn(v[j + u]));
-                                qv[u] = d.fast ? div_rn<true>(d, yv) : div_rn<false>(d, yv);
-                            }
-                            const uint32_t c2 =
-                                __nv_cvt_float2_to_fp8x2(make_float2(qv[0], qv[1]), __NV_SATFINITE, __NV_E4M3);
-                            if (row < mlim) {
-                                const int col = g * 16 + j;
-                                if (col < it.nrows) dst8[(size_t)(it.row0 + col) * a.out_ld] = (uint8_t)c2;
-                                if (col + 1 < it.nrows)
-                                    dst8[(size_t)(it.row0 + col + 1) * a.out_ld] = (uint8_t)(c2 >> 8);
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xfree);  // this warp's reads of the maxima are done
-                ++xph;
+                for (int hh = 0; hh < 2 && ok; ++hh)
+                    if (it.m0 + hh * 128 < mlim) ok = payload_half(it, hh, tl + hh * BN, nb, mlim, sxg, swh[hh]);
+                if (!ok) break;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
