@@ -679,6 +679,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const int mlim = it.shared ? a.m_shared : a.m_routed;
             float sxg[C::kMaxG], swh[2];
             if (MODE == kDownF8Q && !it.shared) payload_scales(it, mlim, sxg, swh);
+            if (MODE == kGateUpF8) {
+                // token scales (one per lane and column group) and the gate and up row
+                // scales of this lane's row, loaded while the MMAs run
+                const float* sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
+#pragma unroll
+                for (int gi = 0; gi < C::kMaxG; ++gi) {
+                    const int col = (part + gi * (kEpiWarps / 4)) * 16 + (lane & 15);
+                    sxg[gi] = col < it.nrows ? __ldg(sbp + col) : 0.0f;
+                }
+                const int r = it.m0 + q * 32 + lane;
+                const size_t zo = (size_t)it.z * (it.shared ? a.m_shared : a.m_routed);
+                swh[0] = r < mlim ? __ldg((it.shared ? a.sa0_scale : a.a0_scale) + zo + r) : 0.0f;
+                swh[1] = r < mlim ? __ldg((it.shared ? a.sa1_scale : a.a1_scale) + zo + r) : 0.0f;
+            }
             if (*abort_flag || !mbar_wait(smem_u32(&tfull[acc]), acc_phase, limit)) {
                 ok = false;
                 break;
@@ -693,14 +707,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 // accumulator (the next item's MMAs may start) and store
                 constexpr int kMaxG = C::kMaxG;
                 uint32_t hp[kMaxG][8];
-                const float* sa0 = nullptr;
-                const float* sa1 = nullptr;
-                const float* sbp = nullptr;
-                if (MODE == kGateUpF8) {
-                    sa0 = it.shared ? a.sa0_scale + (size_t)it.z * a.m_shared : a.a0_scale + (size_t)it.z * a.m_routed;
-                    sa1 = it.shared ? a.sa1_scale + (size_t)it.z * a.m_shared : a.a1_scale + (size_t)it.z * a.m_routed;
-                    sbp = (it.shared ? a.sb_scale : a.b_scale) + it.row0;
-                }
 #pragma unroll
                 for (int gi = 0; gi < kMaxG; ++gi) {
                     const int g = part + gi * (kEpiWarps / 4);
@@ -709,15 +715,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         tmem_ld16(tl + g * 16, v0);
                         tmem_ld16(tl + BN + g * 16, v1);
                         tmem_ld_wait();
-                        if (MODE == kGateUpF8 && row_ok) {
+                        if (MODE == kGateUpF8) {
                             // dequantise: weight-row scale x token scale (both factor out of the K sum)
-                            const float wg = __ldg(sa0 + mrow), wu = __ldg(sa1 + mrow);
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
-                                const int col = g * 16 + j;
-                                const float sx = col < it.nrows ? __ldg(sbp + col) : 0.0f;
-                                v0[j] *= wg * sx;
-                                v1[j] *= wu * sx;
+                                const float sx = __shfl_sync(0xffffffffu, sxg[gi], j);
+                                v0[j] *= swh[0] * sx;
+                                v1[j] *= swh[1] * sx;
                             }
                         }
 #pragma unroll
