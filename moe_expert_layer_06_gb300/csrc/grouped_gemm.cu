@@ -542,28 +542,41 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             };
             // the four warps have read the previous exchange's maxima
             if (xph > 0 && !mbar_wait(xfree, (xph - 1) & 1, limit)) return false;
-#pragma unroll 1
+            // bf16 y of this warp's column groups, packed and kept for pass 2 where the
+            // registers allow it (the 160-row rotating-slot kernel: 95 registers; the
+            // 128-row kernel spilled and reloads the accumulator instead)
+            constexpr bool kKeepY = C::kRot;
+            uint32_t yb[kMaxG][8];
+#pragma unroll
             for (int gi = 0; gi < kMaxG; ++gi) {
                 const int g = part + gi * (kEpiWarps / 4);
-                if (g >= nb) break;
-                float v[16];
-                load_y(g, sxg[gi], v);
-                // rounding is monotone: the bf16 of the largest |y| is the largest bf16 |y|
-                float mine = 0.0f;
+                if (g < nb) {
+                    float v[16];
+                    load_y(g, sxg[gi], v);
+                    // rounding is monotone: the bf16 of the largest |y| is the largest bf16 |y|
+                    float mine = 0.0f;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
-                    if (lane == j) mine = __uint_as_float(mx);
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j])));
+                        if (lane == j) mine = __uint_as_float(mx);
+                    }
+                    if (lane < 16) xw[(gi * 2 + hh) * 16 + lane] = __bfloat162float(__float2bfloat16_rn(mine));
+                    if constexpr (kKeepY) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+                            yb[gi][j] = *reinterpret_cast<const uint32_t*>(&p2);
+                        }
+                    }
                 }
-                if (lane < 16) xw[(gi * 2 + hh) * 16 + lane] = __bfloat162float(__float2bfloat16_rn(mine));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(xfull);
             if (!mbar_wait(xfull, xph & 1, limit)) return false;
-#pragma unroll 1
+#pragma unroll
             for (int gi = 0; gi < kMaxG; ++gi) {
                 const int g = part + gi * (kEpiWarps / 4);
-                if (g >= nb) break;
+                if (g >= nb) continue;
                 // lane l < 16: scale of column l from the four warps' maxima
                 const int o = (gi * 2 + hh) * 16 + (lane & 15);
                 const float amax = fmaxf(fmaxf(xp[o], xp[kMaxG * 32 + o]),
@@ -573,8 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 if (q == 0 && lane < 16 && col_l < it.nrows)
                     a.out8_scale[(size_t)(it.row0 + col_l) * a.n_blk + blk] = sl;
                 const RowDiv dl = row_div(sl);
-                float v[16];
-                load_y(g, sxg[gi], v);
+                if constexpr (!kKeepY) {
+                    float v[16];
+                    load_y(g, sxg[gi], v);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+                        yb[gi][j] = *reinterpret_cast<const uint32_t*>(&p2);
+                    }
+                }
                 // codes of the 16 columns, four to a word (byte c of word b: column 4b + c)
                 uint32_t w[4];
                 auto encode = [&](auto all_fast) {
@@ -586,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                             RowDiv d;
                             d.s = __shfl_sync(0xffffffffu, dl.s, j + u);
                             d.r = __shfl_sync(0xffffffffu, dl.r, j + u);
-                            const float yv = __bfloat162float(__float2bfloat16_rn(v[j + u]));
+                            const uint32_t yw = yb[gi][j >> 1];
+                            const float yv = __uint_as_float(u ? (yw & 0xffff0000u) : (yw << 16));
                             if (decltype(all_fast)::value) qv[u] = div_rn<true>(d, yv);
                             else qv[u] = d.s >= 0x1p-96f ? div_rn<true>(d, yv) : div_rn<false>(d, yv);
                         }
