@@ -756,25 +756,32 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-                if (row_ok) {
-                    uint16_t* dst;
-                    int ld;
+                {
+                    // h as words of two rows: lanes 2m and 2m+1 swap half their columns, so
+                    // the even lane holds the even columns of rows (2m, 2m+1) and the odd lane
+                    // the odd ones (I % 8 == 0: both rows of a pair are valid together)
+                    const bool odd = lane & 1;
+                    const int row2 = mrow & ~1;
+                    uint32_t* dst;
+                    int ldw;
                     if (it.shared) {
-                        dst = reinterpret_cast<uint16_t*>(a.out_sh) + (size_t)it.z * a.sh_col_stride + mrow;
-                        ld = a.out_sh_ld;
+                        dst = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out_sh) +
+                                                          (size_t)it.z * a.sh_col_stride + row2);
+                        ldw = a.out_sh_ld >> 1;
                     } else {
-                        dst = reinterpret_cast<uint16_t*>(a.out) + mrow;
-                        ld = a.out_ld;
+                        dst = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(a.out) + row2);
+                        ldw = a.out_ld >> 1;
                     }
 #pragma unroll
                     for (int gi = 0; gi < kMaxG; ++gi) {
                         const int g = part + gi * (kEpiWarps / 4);
                         if (g < nb) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int col = g * 16 + j;
-                                if (col < it.nrows)
-                                    dst[(size_t)(it.row0 + col) * ld] = (uint16_t)(hp[gi][j >> 1] >> ((j & 1) * 16));
+                            for (int i = 0; i < 8; ++i) {
+                                const uint32_t o = __shfl_xor_sync(0xffffffffu, hp[gi][i], 1);
+                                const uint32_t w = __byte_perm(hp[gi][i], o, odd ? 0x3276 : 0x5410);
+                                const int col = g * 16 + 2 * i + (odd ? 1 : 0);
+                                if (row_ok && col < it.nrows) dst[(size_t)(it.row0 + col) * ldw] = w;
                             }
                         }
                     }
@@ -819,6 +826,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 #pragma unroll
                 for (int hh = 0; hh < NA; ++hh) {
                     const int row = mrow + hh * 128;
+                    if (MODE == kDown && !it.shared) {
+                        // bf16 y as words of two rows: lanes 2m and 2m+1 swap half their
+                        // columns, so the even lane holds the even columns of rows (row,
+                        // row+1) and the odd lane the odd ones (H % 8 == 0: both rows of a
+                        // pair are valid together, and every word is 4-byte aligned)
+                        const bool odd = lane & 1;
+                        uint32_t* dst = reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(a.out) + (row & ~1));
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float* vv = hh ? v1 : v0;
+                            const __nv_bfloat162 p2 = __floats2bfloat162_rn(vv[2 * i], vv[2 * i + 1]);
+                            const uint32_t p = *reinterpret_cast<const uint32_t*>(&p2);
+                            const uint32_t o = __shfl_xor_sync(0xffffffffu, p, 1);
+                            const uint32_t w = __byte_perm(p, o, odd ? 0x3276 : 0x5410);
+                            const int col = g * 16 + 2 * i + (odd ? 1 : 0);
+                            if (row < mlim && col < it.nrows) dst[(size_t)(it.row0 + col) * (a.out_ld >> 1)] = w;
+                        }
+                        continue;
+                    }
                     if (row >= mlim) continue;
                     if (Traits<MODE>::kDownF8Like) {
                         // dequantise: weight-row scale x intermediate-row scale
