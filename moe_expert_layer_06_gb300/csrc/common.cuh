@@ -141,6 +141,21 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Global stores with an L2 eviction-priority hint (a policy from createpolicy).
+__device__ __forceinline__ void st_hint(uint32_t* p, uint32_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ void st_hint(uint2* p, uint2 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ void st_hint(uint4* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 // 3-D tiled load; c0 is the innermost (contiguous) coordinate in elements.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
                                             int c1, int c2, uint64_t policy) {

@@ -762,6 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     // the odd ones (I % 8 == 0: both rows of a pair are valid together)
                     const bool odd = lane & 1;
                     const int row2 = mrow & ~1;
+                    // the down projection reads h next: keep it in L2 ahead of the streamed weights
+                    const uint64_t pol_h = policy_evict_last();
                     uint32_t* dst;
                     int ldw;
                     if (it.shared) {
@@ -781,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                                 const uint32_t o = __shfl_xor_sync(0xffffffffu, hp[gi][i], 1);
                                 const uint32_t w = __byte_perm(hp[gi][i], o, odd ? 0x3276 : 0x5410);
                                 const int col = g * 16 + 2 * i + (odd ? 1 : 0);
-                                if (row_ok && col < it.nrows) dst[(size_t)(it.row0 + col) * ldw] = w;
+                                if (row_ok && col < it.nrows) st_hint(dst + (size_t)(it.row0 + col) * ldw, w, pol_h);
                             }
                         }
                     }
