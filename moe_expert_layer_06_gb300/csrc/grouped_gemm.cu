@@ -22,8 +22,11 @@
 // host synchronisation is needed.  A persistent CTA per SM takes items
 // round-robin; warp roles:
 //   warp 0      TMA producer (one elected lane)   smem ring of STAGES stages
-//   warp 1      MMA issuer   (one elected lane)   TMEM accumulators (x2 when they fit)
-//   warps 2..17 epilogue: tcgen05.ld -> SwiGLU / convert -> global stores
+//   warp 1      MMA issuer   (one elected lane)   TMEM accumulators: two when they
+//                                                 fit; the 160-row E4M3 down rotates
+//                                                 three one-tile slots instead
+//   warps 2..17 epilogue: tcgen05.ld -> SwiGLU / dequantise / E4M3 payload ->
+//               global stores (bf16 as two-row words, payload codes as words)
 // Every mbarrier wait is bounded; on expiry the kernel raises the status word,
 // drains its own copies and MMAs (bounded) and frees its TMEM.
 #include <cuda_fp8.h>
