@@ -191,7 +191,9 @@ def layer_bytes_flops(w, counts_np, fp8=False):
 # ------------------------------------------------------------------------------ our arm
 
 # workloads timed after the headline one, in the same run and with the same step count
-EXTRA_CONFIGS = ("decode_t256_skew", "prefill_t4096", "redundant_t1024")
+# (decode_t256_skew_a05: the skewed batch with the bias calibrated to the pages'
+# ~30% of experts taking ~60% of the assignments, beside the literal formula)
+EXTRA_CONFIGS = ("decode_t256_skew", "decode_t256_skew_a05", "prefill_t4096", "redundant_t1024")
 
 
 class DeviceWeights:

@@ -193,6 +193,11 @@ WORKLOADS = {
                         description="DeepSeek-V3 MoE layer decode step, T=32, near-uniform routing"),
     "decode_t256_skew": _dsv3("decode_t256_skew", 256, 1.5,
                               description="decode T=256, long-tail routing bias 1.5*log(1/(rank+1))"),
+    # the same batch with the bias calibrated to the pages' load picture (about 30% of
+    # the experts take about 60% of the assignments); the literal 1.5 gives ~98%
+    "decode_t256_skew_a05": _dsv3("decode_t256_skew_a05", 256, 0.5,
+                                  description="decode T=256, routing bias 0.5*log(1/(rank+1)): ~30% of "
+                                              "the experts take ~60% of the assignments"),
     "prefill_t4096": _dsv3("prefill_t4096", 4096, 0.0,
                            description="prefill T=4096 (one 4k-token prompt), uniform routing"),
     "redundant_t1024": _dsv3("redundant_t1024", 1024, 1.5, n_slots=264,

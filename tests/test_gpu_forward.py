@@ -101,7 +101,7 @@ def _check_full(w, r, weights, rep=None, n_sample=SAMPLE_TOKENS):
                                  n_sample=n_sample)
 
 
-@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew", "prefill_t4096"])
+@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew", "decode_t256_skew_a05", "prefill_t4096"])
 def test_forward_full_size(name, dsv3_weights):
     """The layer at the bench's launch configuration: every token's routing,
     the counts of the GPU's own routing, and 256 seeded random tokens' outputs

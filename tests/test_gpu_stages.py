@@ -27,7 +27,7 @@ DEEP = mi.WORKLOADS["tiny"].with_(name="deep", tokens=600, hidden=136, inter=264
 REP = mi.WORKLOADS["tiny"].with_(name="rep", tokens=64, hidden=128, inter=64, n_experts=8, top_k=2,
                                  n_shared=1, inter_shared=64, n_slots=12, n_blocks=4)
 SMALL = {"tiny": mi.WORKLOADS["tiny"], "mid": MID, "deep": DEEP}
-FULL = ["decode_t32", "decode_t256_skew", "prefill_t4096", "redundant_t1024"]
+FULL = ["decode_t32", "decode_t256_skew", "decode_t256_skew_a05", "prefill_t4096", "redundant_t1024"]
 
 
 def _wl(name):
