@@ -342,8 +342,10 @@ def _replica_plan_of_skewed_batch(w):
 # decode T=32 runs the 32-row chunk, the skewed T=256 batch the 160-row gate/up
 # and the 128-row down chunk of the automatic mode (hot experts hold more than
 # one), prefill T=4096 the 160-row chunks with the chunked index pass, the
-# redundant T=1024 batch the replica slots
-@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew", "prefill_t4096", "redundant_t1024"])
+# redundant T=1024 batch the replica slots; the calibrated skew touches every expert
+# with at most 65 rows
+@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew", "decode_t256_skew_a05", "prefill_t4096",
+                                  "redundant_t1024"])
 def test_fp8_layer_full_shape(name, dsv3_bf16, fp8_dsv3):
     """The E4M3 layer at the bench's launch configuration against the oracle's
     E4M3 layer: every token's routing, the counts of the GPU's own routing, and
