@@ -38,11 +38,11 @@
  *     atomics, the error text is per thread, and the device status word is
  *     shared (one thread's moe_check_status may report and clear another's
  *     error).  moe_expert_ffn_noalloc calls must not overlap (one scratch).
- *   - Calls enqueue kernels only and may be captured in a CUDA graph.  The
- *     first use of each kernel on a device sets its shared-memory attribute
- *     (cudaFuncSetAttribute, a host-side setting, not a graph node): make
- *     the same call (same entry point, shape and T) once before capturing
- *     it, as a warm-up does.
+ *   - Calls enqueue kernels only.  moe_forward and moe_forward_fp8 replay
+ *     from a captured CUDA graph (tested).  The first use of each kernel on
+ *     a device sets its shared-memory attribute (cudaFuncSetAttribute, a
+ *     host-side setting, not a graph node): make the same call (same entry
+ *     point, shape and T) once before capturing it, as a warm-up does.
  *   - Calls of at most 8192 token-expert assignments (T*k) launch their
  *     kernels with programmatic dependent launch: a kernel may be scheduled
  *     while its predecessor in the stream finishes and waits for it before
