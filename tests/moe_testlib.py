@@ -357,14 +357,17 @@ def oracle_sampled_layer(w, toks, x_cpu, idx, weight, expert_host, shared, fp8=F
 
 
 def check_full_size_layer(w, out_gpu, idx_gpu, counts_gpu, blocks_gpu, expert_host, shared, rep=None, fp8=False,
-                          n_sample=SAMPLE_TOKENS, what=""):
+                          n_sample=SAMPLE_TOKENS, what="", x=None):
     """Parity of a full-size layer pass against the oracle.
 
     Routing of every token (oracle logits in fp64 on the host threads): top-k
     sets and order where decided; counts and block loads of the GPU's own
     routing, unconditionally.  Output: n_sample seeded random tokens with a
-    decided selection, element by element.  Returns the report record."""
-    x = mi.hidden_states(w)
+    decided selection, element by element.  x: the layer input the GPU ran
+    (default: the workload's generated hidden states).  Returns the report
+    record."""
+    if x is None:
+        x = mi.hidden_states(w)
     wr = mi.router_weight(w)
     b = mi.router_bias(w)
     lo = parallel_router_logits(w, x, wr, b)

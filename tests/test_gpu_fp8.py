@@ -350,6 +350,19 @@ def test_fp8_layer_full_shape(name, dsv3_bf16, fp8_dsv3):
     """The E4M3 layer at the bench's launch configuration against the oracle's
     E4M3 layer: every token's routing, the counts of the GPU's own routing, and
     256 seeded random tokens' outputs (all 32 at T=32) element by element."""
+    _fp8_full_shape(name, dsv3_bf16, fp8_dsv3, mi.hidden_states(mi.WORKLOADS[name]))
+
+
+@pytest.mark.parametrize("name", ["decode_t32", "decode_t256_skew_a05"])
+def test_fp8_layer_full_shape_with_outlier_tokens(name, dsv3_bf16, fp8_dsv3):
+    """As above with two planted 8-20 sigma entries in every token row, so that
+    each row's E4M3 scale is set by an outlier and the rest of the row
+    quantises coarsely (the case per-row scaling is weakest at)."""
+    x = mi.with_outliers(mi.hidden_states(mi.WORKLOADS[name]), seed=77)
+    _fp8_full_shape(name, dsv3_bf16, fp8_dsv3, x, what=f"{name} E4M3 with outliers")
+
+
+def _fp8_full_shape(name, dsv3_bf16, fp8_dsv3, x, what=None):
     w = mi.WORKLOADS[name]
     T, H, k, S = w.tokens, w.hidden, w.top_k, w.n_slots
     d = dict(fp8_dsv3)
@@ -359,7 +372,6 @@ def test_fp8_layer_full_shape(name, dsv3_bf16, fp8_dsv3):
         se = torch.from_numpy(mi.slot_experts(w, rep)).to(DEV)
         for key in ("qg", "sg", "qu", "su", "qd", "sd"):
             d[key] = d[key].index_select(0, se)
-    x = mi.hidden_states(w)
     b = mi.router_bias(w)
     i32 = dict(dtype=torch.int32, device=DEV)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
@@ -381,4 +393,4 @@ def test_fp8_layer_full_shape(name, dsv3_bf16, fp8_dsv3):
     qsh["qsd"], qsh["ssd"] = oracle.quantize_rows_e4m3(oracle.shared_down_matrix(sdc))
     check_full_size_layer(w, to_np(out), idx.cpu().numpy(), counts.cpu().numpy(), blocks.cpu().numpy(),
                           lambda e: tuple(t[e].cpu() for t in dsv3_bf16), qsh, rep=rep, fp8=True,
-                          what=f"{name} E4M3 sampled out")
+                          what=what or f"{name} E4M3 sampled out", x=x)
