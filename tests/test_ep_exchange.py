@@ -129,3 +129,47 @@ def test_ep_plan_hand_case():
     bad[1] = -1
     with pytest.raises(m.MoeError):
         m.moe_ep_plan(w, 4, bad, recv)
+
+
+def _plan_by_definition(counts, recv, world, spb):
+    """The plan written out from its definition: the rows of source s for local
+    slot j arrive in source order, each source's rows in slot order; the
+    regrouped layout lists slot 0's rows from source 0, 1, ..., then slot 1's."""
+    send = [int(counts[r * spb:(r + 1) * spb].sum()) for r in range(world)]
+    recv_rows = [int(recv[s].sum()) for s in range(world)]
+    src_pos = {}  # (source, slot, i) -> source-major position
+    pos = 0
+    for s_ in range(world):
+        for j in range(spb):
+            for i in range(int(recv[s_, j])):
+                src_pos[(s_, j, i)] = pos
+                pos += 1
+    slot_from_src, offsets = [], [0]
+    for j in range(spb):
+        for s_ in range(world):
+            for i in range(int(recv[s_, j])):
+                slot_from_src.append(src_pos[(s_, j, i)])
+        offsets.append(len(slot_from_src))
+    return send, recv_rows, offsets + [len(slot_from_src)], slot_from_src
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_ep_plan_matches_its_definition_on_random_counts(seed):
+    """Random world sizes, slots per rank and counts (empty slots and sources
+    included) against the plan written out row by row."""
+    rng = np.random.default_rng([7, seed])
+    world = int(rng.choice([1, 2, 4, 8]))
+    spb = int(rng.integers(1, 9))
+    S = world * spb
+    w = mi.WORKLOADS["tiny"].with_(n_experts=S, n_slots=S, n_blocks=world)
+    zero = rng.random(2 * S + 1) < 0.3
+    counts = np.where(zero[:S + 1], 0, rng.integers(0, 40, S + 1)).astype(np.int32)
+    recv = np.where(zero[S + 1:S + 1 + S].reshape(world, spb), 0,
+                    rng.integers(0, 40, (world, spb))).astype(np.int32)
+    p = m.moe_ep_plan(w, world, counts, recv)
+    send, recv_rows, offsets, sfs = _plan_by_definition(counts, recv, world, spb)
+    assert p["send_rows"].tolist() == send
+    assert p["recv_rows"].tolist() == recv_rows and p["rows"] == len(sfs)
+    assert p["local_offsets"].tolist() == offsets
+    assert p["slot_from_src"].tolist() == sfs
+    assert np.array_equal(p["src_from_slot"][p["slot_from_src"]], np.arange(len(sfs)))
